@@ -1,0 +1,396 @@
+"""Benchmark of the NVFP4 linear layer hot path at Llama-3-8B MLP up-projection
+shapes: x bf16[16384,4096], W bf16[14336,4096], dy bf16[16384,14336].
+
+One step = the whole path once: amax + fused row/col quantization of x (RHT on
+the columnwise copy) and W, the forward GEMM, amax + quantization of dy
+(stochastic rounding, RHT on the columnwise copy), the dgrad and the wgrad
+GEMMs (3 x 2*16384*14336*4096 = 5.77 TFLOP).  Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the CPU oracle (plain C, OpenMP) on a bounded sample
+of the same workload on the host cores.  With N > 1 (torchrun), every rank
+runs an independent replica on its own GPU (the path needs no exchange at one
+GPU per replica); the value is the sum over ranks, the time the max.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+M, N, K = 16384, 14336, 4096
+GEMM_FLOP = 2.0 * M * N * K
+STEP_FLOP = 3 * GEMM_FLOP
+METRIC = "NVFP4 linear fwd+dgrad+wgrad TFLOP/s (Llama-3-8B MLP up-proj)"
+UNIT = "TFLOP/s"
+CONFIG = {"workload": "llama3_8b_mlp_up_fwd_dgrad_wgrad", "M_tokens": M, "N_out": N, "K_in": K,
+          "x": "bf16[16384,4096] N(0,1) seed 0", "W": "bf16[14336,4096] N(0,0.02^2) seed 1",
+          "dy": "bf16[16384,14336] N(0,1e-4) seed 2", "sr_seed": 1234, "rht_sign_seed": 7,
+          "l2": "inputs larger than L2 (each step streams > 1.5 GB through HBM)"}
+# fp4 dense / bf16 dense nominal ratio (13.5 / 2.25 PFLOP/s) applied to the measured bf16 peak
+FP4_OVER_BF16 = 6.0
+
+
+def _env_int(name, default):
+    try:
+        return int(os.environ.get(name, default))
+    except ValueError:
+        return default
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    except OSError:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.out, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------- CPU oracle sample
+def oracle_sample(x, w, dy, sign, rows=64, tile=64):
+    """Time the oracle on a bounded sample of one step and extrapolate to the
+    whole step: quantization of `rows` rows (row + col, as in the step) of each
+    tensor scaled by element count, plus one tile x tile output block of each
+    GEMM (dequantize + fp64 product) scaled by FLOPs.  Returns (TFLOP/s, desc, threads)."""
+    import numpy as np
+    import oracle
+
+    def bits(t):
+        import torch
+        return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+    xb, wb, dyb = bits(x[:rows]), bits(w[:rows]), bits(dy[:rows])
+    t0 = time.perf_counter()
+    A = oracle.amax(xb)
+    xr = oracle.nvfp4_quantize_rows(xb, A=A)
+    xc = oracle.nvfp4_quantize_cols(xb, rht_sign=sign)
+    Aw = oracle.amax(wb)
+    wr = oracle.nvfp4_quantize_rows(wb, A=Aw)
+    wc = oracle.nvfp4_quantize_cols(wb)
+    Ad = oracle.amax(dyb)
+    dr = oracle.nvfp4_quantize_rows(dyb, A=Ad, sr=(1234, 0))
+    dc = oracle.nvfp4_quantize_cols(dyb, rht_sign=sign, sr=(1234, 0))
+    t_q = time.perf_counter() - t0
+    q_scale = (M * K + N * K + M * N) / float(rows * (K + K + N))
+
+    def deq(t, n):
+        c, s, a = t
+        return oracle.nvfp4_dequant(c[:n], s[:n], oracle.nvfp4_g(a))
+
+    t0 = time.perf_counter()
+    oracle.gemm_tn_f64(deq(xr, tile), deq(wr, tile))             # fwd tile, contraction K
+    oracle.gemm_tn_f64(deq(dr, tile), deq(dr, tile))             # dgrad-shaped tile, contraction N
+    ext = oracle.gemm_tn_f64(deq(dc, tile), deq(xc, tile))       # wgrad-shaped tile, contraction rows
+    t_g = time.perf_counter() - t0
+    g_flop = 2.0 * tile * tile * (K + N + rows)
+    g_scale = STEP_FLOP / g_flop
+    t_step = t_q * q_scale + t_g * g_scale
+    threads = _env_int("OMP_NUM_THREADS", os.cpu_count() or 1)
+    desc = (f"oracle on {rows} rows of x/W/dy (amax, row+col quantize with RHT/SR as in the step) "
+            f"extrapolated x{q_scale:.0f} by elements, plus one {tile}x{tile} tile of each GEMM "
+            f"(dequantize + fp64) extrapolated x{g_scale:.3g} by FLOPs; measured {t_q + t_g:.2f} s")
+    del ext
+    return STEP_FLOP / t_step / 1e12, desc, threads, t_q + t_g
+
+
+# ---------------------------------------------------------------- reference arm
+def run_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    from mxfp8_block_scaled_bf16_gb300 import inputs
+    x, w, dy = inputs.llama_up()
+    sign = inputs.rht_sign_vector()
+    vals, secs = [], []
+    for i in range(args.warmup + args.steps):
+        v, desc, threads, s = oracle_sample(x, w, dy, sign)
+        if i >= args.warmup:
+            vals.append(v)
+            secs.append(s)
+    value = statistics.median(vals)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": STEP_FLOP / (value * 1e12) * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "nvfp4 (oracle: f32 encode, f64 GEMM)",
+            "data": "synthetic", "config": CONFIG,
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------- our arm
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    import __graft_entry__
+    import mxfp8_block_scaled_bf16_gb300 as nvq
+    from mxfp8_block_scaled_bf16_gb300 import inputs
+
+    __graft_entry__.build()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    x_h, w_h, dy_h = inputs.llama_up()
+    sign = inputs.rht_sign_vector()
+    sr = (inputs.SR_SEED, 0)
+    x, w, dy = x_h.to(dev), w_h.to(dev), dy_h.to(dev)
+    alloc = nvq.alloc_qtensor
+    cc = nvq.colwise_cols
+    fwd_bufs = dict(x_row=alloc(nvq.NVFP4, M, K, device=dev), w_row=alloc(nvq.NVFP4, N, K, device=dev),
+                    x_col=alloc(nvq.NVFP4, K, cc(nvq.NVFP4, M), device=dev),
+                    w_col=alloc(nvq.NVFP4, K, cc(nvq.NVFP4, N), device=dev))
+    bwd_bufs = dict(dy_row=alloc(nvq.NVFP4, M, N, device=dev), dy_col=alloc(nvq.NVFP4, N, cc(nvq.NVFP4, M), device=dev))
+    y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+    dx = torch.empty(M, K, dtype=torch.bfloat16, device=dev)
+    dw = torch.empty(N, K, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    gemm_events = []
+
+    def step(record):
+        # forward: amax + fused quantize of x (row, col+RHT) and W (row, col), GEMM
+        nvq.nvfp4_quantize(x, 3, rht_sign=sign, out_row=fwd_bufs["x_row"], out_col=fwd_bufs["x_col"])
+        nvq.nvfp4_quantize(w, 3, out_row=fwd_bufs["w_row"], out_col=fwd_bufs["w_col"])
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)] if record else None
+        if record:
+            ev[0].record(stream)
+        nvq.gemm_tn(fwd_bufs["x_row"], fwd_bufs["w_row"], out=y)
+        if record:
+            ev[1].record(stream)
+        # backward: quantize dy (row + col, SR, RHT on col), dgrad, wgrad
+        nvq.nvfp4_linear_bwd_quantize(dy, rht_sign=sign, sr=sr, bufs=bwd_bufs)
+        if record:
+            ev[2].record(stream)
+        nvq.nvfp4_linear_dgrad(bwd_bufs["dy_row"], fwd_bufs["w_col"], dx=dx)
+        if record:
+            ev[3].record(stream)
+            ev[4].record(stream)
+        nvq.nvfp4_linear_wgrad(bwd_bufs["dy_col"], fwd_bufs["x_col"], dw=dw)
+        if record:
+            ev[5].record(stream)
+            gemm_events.append(ev)
+
+    for _ in range(args.warmup):
+        step(False)
+    torch.cuda.synchronize()
+    if nvq.device_status() != 0:
+        raise RuntimeError("device status error during warm-up")
+
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        step(True)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    ms = t0.elapsed_time(t1) / args.steps
+    gemm_ms = [ev[0].elapsed_time(ev[1]) for ev in gemm_events]
+    dgrad_ms = [ev[2].elapsed_time(ev[3]) for ev in gemm_events]
+    wgrad_ms = [ev[4].elapsed_time(ev[5]) for ev in gemm_events]
+    avg_gemm_ms = statistics.mean(gemm_ms + dgrad_ms + wgrad_ms)
+    status = nvq.device_status()
+    if status != 0:
+        raise RuntimeError(f"device status {status} after the timed region")
+
+    # whole-step device time, max over ranks
+    t = torch.tensor([ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_max = float(t.item())
+    value = world * STEP_FLOP / (ms_max * 1e-3) / 1e12
+
+    # quantize-only throughput (x, W, dy: amax pass + fused row/col pass)
+    q_ms = time_quantize(nvq, x, w, dy, sign, sr, fwd_bufs, bwd_bufs, stream)
+
+    e2e = measure_e2e(args, nvq, x_h, w_h, dy_h, sign, sr, dev, stream, world) if not args.no_e2e else None
+
+    if rank != 0:
+        return 0
+    peaks, src = _peaks()
+    peak_fp4 = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")) * FP4_OVER_BF16
+    achieved = GEMM_FLOP / (avg_gemm_ms * 1e-3) / 1e12
+    q_bytes = (M * K + N * K + M * N) * 5.125  # 2 reads of bf16 + 2 x (codes + scales) writes
+    q_gbs = q_bytes / (q_ms * 1e-3) / 1e9
+    cpu_v, cpu_desc, cpu_threads, _ = oracle_sample(x_h, w_h, dy_h, sign)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "nvfp4", "data": "synthetic", "config": CONFIG,
+        "gpu_launches": 9 * args.steps,
+        "roofline": {"bound": "tensor", "kernel": "gemm_kernel<NVFP4> (fwd, dgrad, wgrad)",
+                     "achieved": achieved, "peak": peak_fp4, "unit": "TFLOP/s", "frac": achieved / peak_fp4,
+                     "traffic": None,
+                     "peak_note": f"{src} bf16 sustained x {FP4_OVER_BF16} (fp4/bf16 nominal dense ratio)"},
+        "roofline_quantize": {"bound": "hbm", "achieved": q_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                              "frac": q_gbs / peaks["hbm_gbs"], "traffic": None,
+                              "algorithmic_bytes": q_bytes, "peak_note": f"{src} HBM copy"},
+        "breakdown_ms": {"step": ms_max, "gemm_fwd": statistics.mean(gemm_ms), "gemm_dgrad": statistics.mean(dgrad_ms),
+                         "gemm_wgrad": statistics.mean(wgrad_ms), "quantize_x_w_dy": q_ms},
+        "clocks": clk,
+        "cpu_baseline": {"value": cpu_v, "unit": UNIT, "cores": cpu_threads, "kind": "oracle", "sample": cpu_desc},
+        "e2e": e2e,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def time_quantize(nvq, x, w, dy, sign, sr, fb, bb, stream, reps=5):
+    import torch
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for _ in range(reps):
+        nvq.nvfp4_quantize(x, 3, rht_sign=sign, out_row=fb["x_row"], out_col=fb["x_col"])
+        nvq.nvfp4_quantize(w, 3, out_row=fb["w_row"], out_col=fb["w_col"])
+        nvq.nvfp4_linear_bwd_quantize(dy, rht_sign=sign, sr=sr, bufs=bb)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    return t0.elapsed_time(t1) / reps
+
+
+def measure_e2e(args, nvq, x_h, w_h, dy_h, sign, sr, dev, stream, world):
+    """Same step through the public linear API with host inputs: pinned host ->
+    device copies of x, W, dy and device -> host copies of y, dx, dW inside the
+    timed region."""
+    import torch
+    xh, wh, dyh = x_h.pin_memory(), w_h.pin_memory(), dy_h.pin_memory()
+    yh = torch.empty(M, N, dtype=torch.bfloat16).pin_memory()
+    dxh = torch.empty(M, K, dtype=torch.bfloat16).pin_memory()
+    dwh = torch.empty(N, K, dtype=torch.bfloat16).pin_memory()
+    xd, wd, dyd = torch.empty_like(xh, device=dev), torch.empty_like(wh, device=dev), torch.empty_like(dyh, device=dev)
+    y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+    fb = bb = None
+
+    def step():
+        nonlocal fb, bb
+        xd.copy_(xh, non_blocking=True)
+        wd.copy_(wh, non_blocking=True)
+        dyd.copy_(dyh, non_blocking=True)
+        _, fb = nvq.nvfp4_linear_fwd(xd, wd, rht_sign=sign, y=y, bufs=fb)
+        bb = nvq.nvfp4_linear_bwd_quantize(dyd, rht_sign=sign, sr=sr, bufs=bb)
+        dx = nvq.nvfp4_linear_dgrad(bb["dy_row"], fb["w_col"])
+        dw = nvq.nvfp4_linear_wgrad(bb["dy_col"], fb["x_col"])
+        yh.copy_(y, non_blocking=True)
+        dxh.copy_(dx, non_blocking=True)
+        dwh.copy_(dw, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    steps = max(1, min(args.steps, 10))
+    for _ in range(steps):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / steps
+    bi = (M * K + N * K + M * N) * 2
+    bo = (M * N + M * K + N * K) * 2
+    return {"value": world * STEP_FLOP / (ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": ms,
+            "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
+            "api": "nvq_nvfp4_linear_fwd / _bwd_quantize / _dgrad / _wgrad with pinned host buffers"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3) if args.impl == "ours" else args.warmup
+    world = _env_int("WORLD_SIZE", 1)
+    rank = _env_int("RANK", 0)
+    local_rank = _env_int("LOCAL_RANK", 0)
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+    if world > 1:
+        import torch.distributed as dist
+        import torch
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    try:
+        return run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,452 @@
+// quantize.cu -- amax pass and fused rowwise + columnwise block quantization
+// of bf16 tensors into NVFP4 (E2M1 + E4M3 1x16 scales + FP32 tensor scale) and
+// MXFP8 (E4M3 + E8M0 1x32 scales), with the optional 16-point random Hadamard
+// transform on the columnwise blocks and Philox stochastic rounding.
+//
+// Method: "Add an NVFP4 quantization converter" (torchtitan PR #3914, "What
+// changed"; review thread on "rowwise") and "Hybrid quantization"
+// (TransformerEngine PR #2817, "Description", mxfp8 storage review).
+//
+// Work decomposition (both kernels): a CTA owns a tile of 128 (padded) rows x
+// 256 columns; warp w covers rows 32*(w&3).. and columns 128*(w>>2)..; lane l
+// owns 16 consecutive rows (half (l>>4) of the warp's 32) x 8 consecutive
+// columns (group l&15).  One 16-byte load per row brings a thread's 8 bf16
+// values, so every element is read from HBM once per pass and held in
+// registers: a columnwise 16-block lives entirely in one thread (Hadamard
+// butterflies in registers), a rowwise 16-block spans a lane pair (one
+// shuffle), a 32-block spans 4 lanes (rows) or a lane and lane^16 (columns).
+// Outputs that are not contiguous per thread (transposed codes, swizzled
+// scales) are staged in shared memory and written out with vector stores.
+//
+// Grouped tensors: rows are addressed in a padded space where each group
+// starts at a multiple of 128, so no tile straddles two groups; rows of the
+// padded space with no source row read as zero.
+#include "nvq_kernels.h"
+#include "nvq_device.cuh"
+
+namespace nvq {
+
+constexpr int kTileRows = 128;
+constexpr int kTileCols = 256;
+constexpr int kThreads = 256;
+
+struct ThreadTile {
+    uint4 w[16];  // 16 rows x 8 bf16
+};
+
+__device__ __forceinline__ int find_group(const QuantGroups& g, int64_t tile_row)
+{
+    int lo = 0, hi = g.G - 1;
+    while (lo < hi) {  // last group whose first tile <= tile_row
+        const int mid = (lo + hi + 1) >> 1;
+        if (g.tile0[mid] <= tile_row) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
+}
+
+// Loads the thread's 16 x 8 block; rows with no source row (padding) and
+// columns >= K read as zero.
+__device__ __forceinline__ void load_tile(const QuantArgs& a, int g, int64_t prow0, int64_t k0,
+                                          ThreadTile& t)
+{
+    const int64_t gp0 = (int64_t)a.groups.tile0[g] * kTileRows;  // padded start of group
+    const int64_t m = a.groups.rows[g];
+    const int64_t src0 = a.groups.src_row0[g];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const int64_t local = prow0 + i - gp0;
+        if (local < m && k0 < a.K) {
+            const uint4* p = reinterpret_cast<const uint4*>(a.x + (src0 + local) * a.ld + k0);
+            t.w[i] = __ldg(p);
+        } else {
+            t.w[i] = make_uint4(0, 0, 0, 0);
+        }
+    }
+}
+
+__device__ __forceinline__ void unpack8(const uint4& w, float (&v)[8])
+{
+    v[0] = bf16_lo(w.x); v[1] = bf16_hi(w.x);
+    v[2] = bf16_lo(w.y); v[3] = bf16_hi(w.y);
+    v[4] = bf16_lo(w.z); v[5] = bf16_hi(w.z);
+    v[6] = bf16_lo(w.w); v[7] = bf16_hi(w.w);
+}
+
+// Column j (0..7) of the thread's tile as 16 fp32 values.
+__device__ __forceinline__ void column16(const ThreadTile& t, int j, float (&u)[16])
+{
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const uint32_t word = (j >> 1) == 0 ? t.w[i].x : (j >> 1) == 1 ? t.w[i].y : (j >> 1) == 2 ? t.w[i].z : t.w[i].w;
+        u[i] = (j & 1) ? bf16_hi(word) : bf16_lo(word);
+    }
+}
+
+// T(u) = 1/4 H16 (s .* u): sign flip, butterflies with spans 1, 2, 4, 8, scale.
+__device__ __forceinline__ void rht16(float (&u)[16], uint32_t sign_mask)
+{
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+        if (sign_mask & (1u << i)) u[i] = -u[i];
+#pragma unroll
+    for (int h = 1; h < 16; h <<= 1) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            if ((i & h) == 0) {
+                const float a = u[i], b = u[i + h];
+                u[i] = __fadd_rn(a, b);
+                u[i + h] = __fsub_rn(a, b);
+            }
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) u[i] = __fmul_rn(u[i], 0.25f);
+}
+
+__device__ __forceinline__ void atomic_max_nonneg(float* addr, float v)
+{
+    atomicMax(reinterpret_cast<unsigned int*>(addr), __float_as_uint(v));
+}
+
+__device__ __forceinline__ float warp_max(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    return v;
+}
+
+// ------------------------------------------------------------------ amax pass
+__global__ void __launch_bounds__(kThreads) amax_kernel(QuantArgs a)
+{
+    const int64_t tile_row = blockIdx.y;
+    const int g = find_group(a.groups, tile_row);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t prow0 = tile_row * kTileRows + (warp & 3) * 32 + (lane >> 4) * 16;
+    const int64_t k0 = (int64_t)blockIdx.x * kTileCols + (warp >> 2) * 128 + (lane & 15) * 8;
+
+    ThreadTile t;
+    load_tile(a, g, prow0, k0, t);
+
+    float m_plain = 0.0f, m_rht = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        float v[8];
+        unpack8(t.w[i], v);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) m_plain = fmaxf(m_plain, fabsf(v[j]));
+    }
+    if (a.amax_rht_out) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            float u[16];
+            column16(t, j, u);
+            rht16(u, a.rht_sign_mask);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) m_rht = fmaxf(m_rht, fabsf(u[i]));
+        }
+    }
+    __shared__ float red[2][kThreads / 32];
+    m_plain = warp_max(m_plain);
+    m_rht = warp_max(m_rht);
+    if (lane == 0) {
+        red[0][warp] = m_plain;
+        red[1][warp] = m_rht;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float p = 0.0f, r = 0.0f;
+        for (int w = 0; w < kThreads / 32; ++w) {
+            p = fmaxf(p, red[0][w]);
+            r = fmaxf(r, red[1][w]);
+        }
+        if (a.amax_out[0]) atomic_max_nonneg(a.amax_out[0] + g, p);
+        if (a.amax_out[1]) atomic_max_nonneg(a.amax_out[1] + g, p);
+        if (a.amax_rht_out) atomic_max_nonneg(a.amax_rht_out + g, r);
+    }
+}
+
+// ------------------------------------------------------------------ NVFP4 block encode
+struct Nvfp4Scale {
+    float r448;   // 448 / A
+    float s_enc;  // 2688 / A  (A = 0 -> 1, overflow -> FLT_MAX)
+    bool zero;    // A == 0
+};
+
+__device__ __forceinline__ Nvfp4Scale nvfp4_tensor_scale(float A)
+{
+    Nvfp4Scale s;
+    s.zero = (A == 0.0f);
+    s.r448 = __fdiv_rn(448.0f, A);
+    float se = __fdiv_rn(2688.0f, A);
+    if (s.zero) se = 1.0f;
+    if (isinf(se)) se = 3.402823466e38f;
+    s.s_enc = se;
+    return s;
+}
+
+// Block scale code and element encode factor for block amax b.
+__device__ __forceinline__ uint32_t nvfp4_block_scale(const Nvfp4Scale& ts, float b, float& e)
+{
+    uint32_t S = 0;
+    if (b != 0.0f && !ts.zero) S = e4m3_rn(__fmul_rn(b, ts.r448));
+    e = 0.0f;
+    if (S != 0) {
+        float q = __fdiv_rn(ts.s_enc, e4m3_to_f32(S));
+        e = isinf(q) ? 3.402823466e38f : q;
+    }
+    return S;
+}
+
+// 8 consecutive elements of one direction's output starting at linear index L0
+// (L0 % 8 == 0): E2M1 codes, element 0 in the low nibble.
+template <bool SR>
+__device__ __forceinline__ uint32_t nvfp4_encode8(const float (&v)[8], float e, uint64_t L0, int dir,
+                                                  const QuantArgs& a)
+{
+    float s[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) s[j] = __fmul_rn(v[j], e);
+    if constexpr (SR) {
+        const uint64_t blk = L0 >> 3;
+        const Philox4 p = philox4x32_10((uint32_t)blk, (uint32_t)(blk >> 32), (uint32_t)dir,
+                                        a.sr_offset, a.sr_key0, a.sr_key1);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) s[j] = e2m1_sr_value(s[j], philox_field(p, j));
+    }
+    return e2m1x8_rn(s);
+}
+
+// ------------------------------------------------------------------ MXFP8 block encode
+__device__ __forceinline__ int mx_exponent(float b)
+{
+    if (b == 0.0f) return -127;
+    const uint32_t bits = __float_as_uint(b);
+    const int ef = (int)((bits >> 23) & 0xFF);
+    int lg;  // floor(log2 b), exact for normals and subnormals
+    if (ef != 0) lg = ef - 127;
+    else lg = -118 - __clz(bits & 0x7FFFFF);  // m * 2^-149 -> (31 - clz(m)) - 149
+    int e = lg - 8;
+    return e < -127 ? -127 : (e > 127 ? 127 : e);
+}
+
+// 2^-e as fp32 for e in [-127, 127] (2^127 is finite; 2^-127 is subnormal).
+__device__ __forceinline__ float exp2_neg(int e)
+{
+    const int p = -e;
+    if (p >= -126) return __uint_as_float((uint32_t)(p + 127) << 23);
+    return __uint_as_float(1u << (p + 149));
+}
+
+// ------------------------------------------------------------------ fused quantize
+// Shared staging: transposed codes and both scale tiles.
+struct QuantSmem {
+    uint8_t col_codes[kTileCols][kTileRows + 16];  // per output row k: up to 128 B (MXFP8) + pad
+    uint8_t row_scales[2048];                      // 128 rows x up to 16 scale cols
+    uint8_t col_scales[2][1024];                   // 2 x (128 k-rows x up to 8 scale cols)
+};
+
+template <int ROW_FMT, int COL_FMT, bool RHT, bool SR>
+__global__ void __launch_bounds__(kThreads) quantize_kernel(QuantArgs a)
+{
+    __shared__ __align__(16) QuantSmem sm;
+    const int64_t tile_row = blockIdx.y, tile_col = blockIdx.x;
+    const int g = find_group(a.groups, tile_row);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int r_loc = (warp & 3) * 32 + (lane >> 4) * 16;  // first of the thread's 16 rows in tile
+    const int c_loc = (warp >> 2) * 128 + (lane & 15) * 8; // first of the thread's 8 cols in tile
+    const int64_t prow0 = tile_row * kTileRows + r_loc;
+    const int64_t k0 = tile_col * kTileCols + c_loc;
+    const bool kvalid = k0 < a.K;
+
+    for (int i = threadIdx.x; i < 2048 / 16; i += kThreads) {
+        reinterpret_cast<uint4*>(sm.row_scales)[i] = make_uint4(0, 0, 0, 0);
+        reinterpret_cast<uint4*>(&sm.col_scales[0][0])[i] = make_uint4(0, 0, 0, 0);
+    }
+
+    ThreadTile t;
+    load_tile(a, g, prow0, k0, t);
+    __syncthreads();  // staging cleared
+
+    // ---------------- rowwise direction
+    if constexpr (ROW_FMT == 1) {  // NVFP4, 16-blocks = lane pair
+        const Nvfp4Scale ts = nvfp4_tensor_scale(a.row_amax[g]);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            float v[8];
+            unpack8(t.w[i], v);
+            float b = 0.0f;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) b = fmaxf(b, fabsf(v[j]));
+            b = fmaxf(b, __shfl_xor_sync(0xFFFFFFFFu, b, 1));
+            float e;
+            const uint32_t S = nvfp4_block_scale(ts, b, e);
+            const int64_t p = prow0 + i;
+            const uint64_t L0 = (uint64_t)p * (uint64_t)a.K + (uint64_t)k0;
+            const uint32_t codes = nvfp4_encode8<SR>(v, e, L0, 0, a);
+            if (kvalid && p < a.row_rows_store)
+                *reinterpret_cast<uint32_t*>(a.row_data + p * (a.K / 2) + k0 / 2) = codes;
+            if ((lane & 1) == 0) {
+                const int r = r_loc + i, c = c_loc / 16;  // scale column within the CTA (0..15)
+                sm.row_scales[(c >> 2) * 512 + (r & 31) * 16 + (r >> 5) * 4 + (c & 3)] = (uint8_t)(kvalid ? S : 0);
+            }
+        }
+    } else if constexpr (ROW_FMT == 2) {  // MXFP8, 32-blocks = 4 lanes
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            float v[8];
+            unpack8(t.w[i], v);
+            float b = 0.0f;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) b = fmaxf(b, fabsf(v[j]));
+            b = fmaxf(b, __shfl_xor_sync(0xFFFFFFFFu, b, 1));
+            b = fmaxf(b, __shfl_xor_sync(0xFFFFFFFFu, b, 2));
+            const int e = mx_exponent(b);
+            const float sc = exp2_neg(e);
+            const uint32_t lo = e4m3x4_rn(__fmul_rn(v[0], sc), __fmul_rn(v[1], sc), __fmul_rn(v[2], sc), __fmul_rn(v[3], sc));
+            const uint32_t hi = e4m3x4_rn(__fmul_rn(v[4], sc), __fmul_rn(v[5], sc), __fmul_rn(v[6], sc), __fmul_rn(v[7], sc));
+            const int64_t p = prow0 + i;
+            if (kvalid && p < a.row_rows_store)
+                *reinterpret_cast<uint2*>(a.row_data + p * a.K + k0) = make_uint2(lo, hi);
+            if ((lane & 3) == 0) {
+                const int r = r_loc + i, c = c_loc / 32;  // 0..7
+                sm.row_scales[(c >> 2) * 512 + (r & 31) * 16 + (r >> 5) * 4 + (c & 3)] = (uint8_t)(kvalid ? (e + 127) : 0);
+            }
+        }
+    }
+
+    // ---------------- columnwise direction (output row = column k, contraction = padded row p)
+    if constexpr (COL_FMT == 1) {  // NVFP4: the thread's 16 rows form one block per column
+        const Nvfp4Scale ts = nvfp4_tensor_scale(a.col_amax[g]);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            float u[16];
+            column16(t, j, u);
+            if constexpr (RHT) rht16(u, a.rht_sign_mask);
+            float b = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) b = fmaxf(b, fabsf(u[i]));
+            float e;
+            const uint32_t S = nvfp4_block_scale(ts, b, e);
+            const int64_t k = k0 + j;
+            const uint64_t Lbase = (uint64_t)k * (uint64_t)a.col_cols_store + (uint64_t)prow0;
+            float h0[8], h1[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) { h0[i] = u[i]; h1[i] = u[i + 8]; }
+            const uint32_t c0 = nvfp4_encode8<SR>(h0, e, Lbase, 1, a);
+            const uint32_t c1 = nvfp4_encode8<SR>(h1, e, Lbase + 8, 1, a);
+            *reinterpret_cast<uint2*>(&sm.col_codes[c_loc + j][r_loc / 2]) = make_uint2(c0, c1);
+            const int kk = c_loc + j;      // output row within CTA (0..255)
+            const int c = r_loc / 16;      // scale column within CTA (0..7)
+            sm.col_scales[kk >> 7][(c >> 2) * 512 + (kk & 31) * 16 + ((kk >> 5) & 3) * 4 + (c & 3)] =
+                (uint8_t)(kvalid ? S : 0);
+        }
+    } else if constexpr (COL_FMT == 2) {  // MXFP8: 32-blocks = this thread's 16 rows + lane^16's
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            float u[16];
+            column16(t, j, u);
+            float b = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) b = fmaxf(b, fabsf(u[i]));
+            b = fmaxf(b, __shfl_xor_sync(0xFFFFFFFFu, b, 16));
+            const int e = mx_exponent(b);
+            const float sc = exp2_neg(e);
+            uint4 q;
+            q.x = e4m3x4_rn(__fmul_rn(u[0], sc), __fmul_rn(u[1], sc), __fmul_rn(u[2], sc), __fmul_rn(u[3], sc));
+            q.y = e4m3x4_rn(__fmul_rn(u[4], sc), __fmul_rn(u[5], sc), __fmul_rn(u[6], sc), __fmul_rn(u[7], sc));
+            q.z = e4m3x4_rn(__fmul_rn(u[8], sc), __fmul_rn(u[9], sc), __fmul_rn(u[10], sc), __fmul_rn(u[11], sc));
+            q.w = e4m3x4_rn(__fmul_rn(u[12], sc), __fmul_rn(u[13], sc), __fmul_rn(u[14], sc), __fmul_rn(u[15], sc));
+            *reinterpret_cast<uint4*>(&sm.col_codes[c_loc + j][r_loc]) = q;
+            if ((lane >> 4) == 0) {
+                const int kk = c_loc + j;
+                const int c = r_loc / 32;  // 0..3
+                sm.col_scales[kk >> 7][(kk & 31) * 16 + ((kk >> 5) & 3) * 4 + (c & 3)] =
+                    (uint8_t)(kvalid ? (e + 127) : 0);
+            }
+        }
+    }
+    __syncthreads();
+
+    // ---------------- write-out of staged outputs
+    const int64_t p_tile0 = tile_row * kTileRows;
+    if constexpr (ROW_FMT != 0) {
+        // this CTA's scale columns: NVFP4 16 (4 tiles), MXFP8 8 (2 tiles), all in tile-row tile_row
+        constexpr int ntiles = ROW_FMT == 1 ? 4 : 2;
+        const int64_t ct0 = tile_col * ntiles;
+        for (int i = threadIdx.x; i < ntiles * 32; i += kThreads) {
+            const int tt = i >> 5;
+            if (ct0 + tt < a.row_scale_ctiles) {
+                uint8_t* dst = a.row_scale + ((tile_row * a.row_scale_ctiles + ct0 + tt) * 512) + (i & 31) * 16;
+                *reinterpret_cast<uint4*>(dst) = reinterpret_cast<const uint4*>(sm.row_scales)[i];
+            }
+        }
+    }
+    if constexpr (COL_FMT != 0) {
+        constexpr int bytes_per_k = COL_FMT == 1 ? kTileRows / 2 : kTileRows;  // codes per output row
+        const int64_t row_bytes = COL_FMT == 1 ? a.col_cols_store / 2 : a.col_cols_store;
+        const int64_t byte0 = COL_FMT == 1 ? p_tile0 / 2 : p_tile0;
+        constexpr int chunks = bytes_per_k / 8;  // 8-byte chunks per output row
+        for (int i = threadIdx.x; i < kTileCols * chunks; i += kThreads) {
+            const int kk = i / chunks, ch = i % chunks;
+            const int64_t k = tile_col * kTileCols + kk;
+            const int64_t off = byte0 + ch * 8;
+            if (k < a.K && off < row_bytes)
+                *reinterpret_cast<uint2*>(a.col_data + k * row_bytes + off) =
+                    *reinterpret_cast<const uint2*>(&sm.col_codes[kk][ch * 8]);
+        }
+        // scales: output rows k (two 128-row tile-rows), scale columns p/16 (NVFP4, 2 tiles) or p/32 (1 tile)
+        constexpr int nct = COL_FMT == 1 ? 2 : 1;
+        const int64_t ct0 = COL_FMT == 1 ? (p_tile0 / 16) / 4 : (p_tile0 / 32) / 4;
+        for (int i = threadIdx.x; i < 2 * nct * 32; i += kThreads) {
+            const int kt = i / (nct * 32), rem = i % (nct * 32), tt = rem >> 5, chunk = rem & 31;
+            const int64_t ktile = tile_col * 2 + kt;  // 128-row tile of the output rows
+            if (ktile * 128 < a.col_scale_rows_pad && ct0 + tt < a.col_scale_ctiles) {
+                uint8_t* dst = a.col_scale + (ktile * a.col_scale_ctiles + ct0 + tt) * 512 + chunk * 16;
+                *reinterpret_cast<uint4*>(dst) =
+                    *reinterpret_cast<const uint4*>(&sm.col_scales[kt][tt * 512 + chunk * 16]);
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------ launchers
+cudaError_t launch_amax(const QuantArgs& a, int64_t row_tiles, cudaStream_t s)
+{
+    dim3 grid((unsigned)((a.K + kTileCols - 1) / kTileCols), (unsigned)row_tiles);
+    amax_kernel<<<grid, kThreads, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+template <int R, int C>
+static cudaError_t launch_q3(const QuantArgs& a, dim3 grid, cudaStream_t s, bool rht, bool sr)
+{
+    if (rht && sr) quantize_kernel<R, C, true, true><<<grid, kThreads, 0, s>>>(a);
+    else if (rht) quantize_kernel<R, C, true, false><<<grid, kThreads, 0, s>>>(a);
+    else if (sr) quantize_kernel<R, C, false, true><<<grid, kThreads, 0, s>>>(a);
+    else quantize_kernel<R, C, false, false><<<grid, kThreads, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quantize(const QuantArgs& a, int row_fmt, int col_fmt, bool rht, bool sr,
+                            int64_t row_tiles, cudaStream_t s)
+{
+    dim3 grid((unsigned)((a.K + kTileCols - 1) / kTileCols), (unsigned)row_tiles);
+    // RHT only reaches an NVFP4 columnwise direction; SR only NVFP4 directions.
+    const bool nv = row_fmt == 1 || col_fmt == 1;
+    rht = rht && col_fmt == 1;
+    sr = sr && nv;
+    switch (row_fmt * 3 + col_fmt) {
+        case 1: return launch_q3<0, 1>(a, grid, s, rht, sr);
+        case 2: return launch_q3<0, 2>(a, grid, s, false, false);
+        case 3: return launch_q3<1, 0>(a, grid, s, false, sr);
+        case 4: return launch_q3<1, 1>(a, grid, s, rht, sr);
+        case 5: return launch_q3<1, 2>(a, grid, s, false, sr);
+        case 6: return launch_q3<2, 0>(a, grid, s, false, false);
+        case 7: return launch_q3<2, 1>(a, grid, s, rht, sr);
+        case 8: return launch_q3<2, 2>(a, grid, s, false, false);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace nvq
