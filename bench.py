@@ -110,11 +110,13 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- CPU oracle sample
-def oracle_sample(x, w, dy, sign, rows=64, tile=64):
+def oracle_sample(x, w, dy, sign, target_s=10.0):
     """Time the oracle on a bounded sample of one step and extrapolate to the
-    whole step: quantization of `rows` rows (row + col, as in the step) of each
-    tensor scaled by element count, plus one tile x tile output block of each
-    GEMM (dequantize + fp64 product) scaled by FLOPs.  Returns (TFLOP/s, desc, threads)."""
+    whole step: quantization of `rows` rows (amax, row + col as in the step) of
+    each tensor scaled by element count, plus one tile x tile output block of
+    each GEMM (dequantize + fp64 product) scaled by FLOPs.  A small calibration
+    pass sizes the sample to take about `target_s` seconds.
+    Returns (TFLOP/s, description, threads, seconds measured)."""
     import numpy as np
     import oracle
 
@@ -122,37 +124,41 @@ def oracle_sample(x, w, dy, sign, rows=64, tile=64):
         import torch
         return t.contiguous().view(torch.int16).numpy().view(np.uint16)
 
-    xb, wb, dyb = bits(x[:rows]), bits(w[:rows]), bits(dy[:rows])
-    t0 = time.perf_counter()
-    A = oracle.amax(xb)
-    xr = oracle.nvfp4_quantize_rows(xb, A=A)
-    xc = oracle.nvfp4_quantize_cols(xb, rht_sign=sign)
-    Aw = oracle.amax(wb)
-    wr = oracle.nvfp4_quantize_rows(wb, A=Aw)
-    wc = oracle.nvfp4_quantize_cols(wb)
-    Ad = oracle.amax(dyb)
-    dr = oracle.nvfp4_quantize_rows(dyb, A=Ad, sr=(1234, 0))
-    dc = oracle.nvfp4_quantize_cols(dyb, rht_sign=sign, sr=(1234, 0))
-    t_q = time.perf_counter() - t0
-    q_scale = (M * K + N * K + M * N) / float(rows * (K + K + N))
-
     def deq(t, n):
         c, s, a = t
         return oracle.nvfp4_dequant(c[:n], s[:n], oracle.nvfp4_g(a))
 
-    t0 = time.perf_counter()
-    oracle.gemm_tn_f64(deq(xr, tile), deq(wr, tile))             # fwd tile, contraction K
-    oracle.gemm_tn_f64(deq(dr, tile), deq(dr, tile))             # dgrad-shaped tile, contraction N
-    ext = oracle.gemm_tn_f64(deq(dc, tile), deq(xc, tile))       # wgrad-shaped tile, contraction rows
-    t_g = time.perf_counter() - t0
+    def run(rows, tile):
+        xb, wb, dyb = bits(x[:rows]), bits(w[:rows]), bits(dy[:rows])
+        t0 = time.perf_counter()
+        xr = oracle.nvfp4_quantize_rows(xb, A=oracle.amax(xb))
+        xc = oracle.nvfp4_quantize_cols(xb, rht_sign=sign)
+        wr = oracle.nvfp4_quantize_rows(wb, A=oracle.amax(wb))
+        oracle.nvfp4_quantize_cols(wb)
+        dr = oracle.nvfp4_quantize_rows(dyb, A=oracle.amax(dyb), sr=(1234, 0))
+        dc = oracle.nvfp4_quantize_cols(dyb, rht_sign=sign, sr=(1234, 0))
+        t_q = time.perf_counter() - t0
+        t0 = time.perf_counter()
+        oracle.gemm_tn_f64(deq(xr, tile), deq(wr, tile))        # fwd-shaped tile, contraction K
+        oracle.gemm_tn_f64(deq(dr, tile), deq(dr, tile))        # dgrad-shaped tile, contraction N
+        oracle.gemm_tn_f64(deq(dc, tile), deq(xc, tile))        # wgrad-shaped tile, contraction rows
+        t_g = time.perf_counter() - t0
+        return t_q, t_g
+
+    r0, g0 = 64, 64
+    tq, tg = run(r0, g0)
+    rows = int(min(M, max(r0, r0 * (0.5 * target_s) / max(tq, 1e-3))))
+    rows = max(16, rows // 16 * 16)
+    tile = int(min(rows, max(g0, g0 * ((0.5 * target_s) / max(tg, 1e-3)) ** (1 / 3))))
+    t_q, t_g = run(rows, tile)
+    q_scale = (M * K + N * K + M * N) / float(rows * (K + K + N))
     g_flop = 2.0 * tile * tile * (K + N + rows)
     g_scale = STEP_FLOP / g_flop
     t_step = t_q * q_scale + t_g * g_scale
     threads = _env_int("OMP_NUM_THREADS", os.cpu_count() or 1)
     desc = (f"oracle on {rows} rows of x/W/dy (amax, row+col quantize with RHT/SR as in the step) "
-            f"extrapolated x{q_scale:.0f} by elements, plus one {tile}x{tile} tile of each GEMM "
+            f"extrapolated x{q_scale:.3g} by elements, plus one {tile}x{tile} tile of each GEMM "
             f"(dequantize + fp64) extrapolated x{g_scale:.3g} by FLOPs; measured {t_q + t_g:.2f} s")
-    del ext
     return STEP_FLOP / t_step / 1e12, desc, threads, t_q + t_g
 
 
@@ -165,7 +171,7 @@ def run_reference(args, rank, world):
     sign = inputs.rht_sign_vector()
     vals, secs = [], []
     for i in range(args.warmup + args.steps):
-        v, desc, threads, s = oracle_sample(x, w, dy, sign)
+        v, desc, threads, s = oracle_sample(x, w, dy, sign, target_s=4.0)
         if i >= args.warmup:
             vals.append(v)
             secs.append(s)

