@@ -288,7 +288,10 @@ def run_ours(args, rank, world, local_rank):
     achieved = GEMM_FLOP / (avg_gemm_ms * 1e-3) / 1e12
     q_bytes = (M * K + N * K + M * N) * 5.125  # 2 reads of bf16 + 2 x (codes + scales) writes
     q_gbs = q_bytes / (q_ms * 1e-3) / 1e9
-    cpu_v, cpu_desc, cpu_threads, _ = oracle_sample(x_h, w_h, dy_h, sign)
+    if args.no_cpu_baseline:
+        cpu_v, cpu_desc, cpu_threads = None, "skipped (--no-cpu-baseline)", 0
+    else:
+        cpu_v, cpu_desc, cpu_threads, _ = oracle_sample(x_h, w_h, dy_h, sign)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
@@ -377,7 +380,8 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end measurement")
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip timing the CPU oracle")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3) if args.impl == "ours" else args.warmup
     world = _env_int("WORLD_SIZE", 1)
