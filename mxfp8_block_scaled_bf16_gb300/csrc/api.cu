@@ -24,24 +24,27 @@ constexpr int kMaxDevices = 64;
 struct DeviceInit {
     std::once_flag once;
     int* status = nullptr;
+    int num_sms = 0;
     cudaError_t err = cudaSuccess;
 };
 DeviceInit g_dev[kMaxDevices];
 
 // Per-device one-time setup: the status word's address and the GEMM
 // kernels' shared-memory limit.
-cudaError_t device_setup(int** status)
+cudaError_t device_setup(int** status, int* num_sms = nullptr)
 {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     DeviceInit& d = g_dev[dev];
-    std::call_once(d.once, [&d]() {
+    std::call_once(d.once, [&d, dev]() {
         d.err = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.status), g_status_word);
+        if (d.err == cudaSuccess) d.err = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev);
         if (d.err == cudaSuccess) d.err = init_gemm_attributes();
     });
     *status = d.status;
+    if (num_sms) *num_sms = d.num_sms;
     return d.err;
 }
 
@@ -64,15 +67,15 @@ EncodeTiledFn encode_fn()
     return fn;
 }
 
-// 2-D uint8 tensor map over [rows][row_bytes] with a 128 x 128-byte box and
-// the 128-byte swizzle the MMA descriptors expect.
-nvq_status make_operand_map(CUtensorMap* map, const void* data, int64_t rows, int64_t row_bytes)
+// 2-D uint8 tensor map over [rows][row_bytes] with a box_rows x 128-byte box
+// and the 128-byte swizzle the MMA descriptors expect.
+nvq_status make_operand_map(CUtensorMap* map, const void* data, int64_t rows, int64_t row_bytes, uint32_t box_rows)
 {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return NVQ_ERR_CUDA;
     cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
-    cuuint32_t box[2] = {128, 128};
+    cuuint32_t box[2] = {128, box_rows};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(data), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -239,7 +242,8 @@ nvq_status quantize_impl(const void* x, int64_t M, int64_t K, int64_t ld, const 
     return cuda_status(launch_quantize(a, (int)row_fmt, (int)col_fmt, rht, sr != nullptr, row_tiles, stream));
 }
 
-nvq_status gemm_prepare(const nvq_qtensor* A, const nvq_qtensor* B, CUtensorMap* am, CUtensorMap* bm, GemmArgs* g)
+nvq_status gemm_prepare(const nvq_qtensor* A, const nvq_qtensor* B, int64_t n_out, CUtensorMap* am, CUtensorMap* bm,
+                        GemmArgs* g)
 {
     if (!A || !B || !A->data || !B->data || !A->scale || !B->scale) return NVQ_ERR_NULL;
     if (A->fmt != B->fmt || !valid_fmt(A->fmt)) return NVQ_ERR_UNSUPPORTED;
@@ -261,10 +265,13 @@ nvq_status gemm_prepare(const nvq_qtensor* A, const nvq_qtensor* B, CUtensorMap*
     g->b_scale_ctiles = scale_ctiles(f, B->cols);
     g->a_amax = A->amax;
     g->b_amax = B->amax;
+    if (n_out % 128) return NVQ_ERR_SHAPE;
+    g->block_n = gemm_block_n(n_out);
+    g->any_k = (A->rows > 0 && A->cols > 0 && B->rows > 0 && B->cols > 0) ? 1 : 0;
     const int64_t eb = f == NVQ_FMT_NVFP4 ? 2 : 1;  // elements per byte
     nvq_status s = NVQ_OK;
-    if (A->rows > 0 && A->cols > 0) s = make_operand_map(am, A->data, A->rows, A->cols / eb);
-    if (s == NVQ_OK && B->rows > 0 && B->cols > 0) s = make_operand_map(bm, B->data, B->rows, B->cols / eb);
+    if (g->any_k) s = make_operand_map(am, A->data, A->rows, A->cols / eb, 128);
+    if (s == NVQ_OK && g->any_k) s = make_operand_map(bm, B->data, B->rows, B->cols / eb, (uint32_t)g->block_n);
     return s;
 }
 
@@ -280,9 +287,10 @@ nvq_status check_c(const void* C, int64_t ldc, int64_t ncols, int c_fp32)
 nvq_status gemm_launch(const CUtensorMap& am, const CUtensorMap& bm, GemmArgs& g, cudaStream_t stream)
 {
     int* status = nullptr;
-    if (device_setup(&status) != cudaSuccess) return NVQ_ERR_CUDA;
+    int num_sms = 0;
+    if (device_setup(&status, &num_sms) != cudaSuccess) return NVQ_ERR_CUDA;
     g.status = status;
-    return cuda_status(launch_gemm(&am, &bm, g, stream));
+    return cuda_status(launch_gemm(&am, &bm, g, num_sms, stream));
 }
 
 }  // namespace
@@ -376,11 +384,11 @@ nvq_status nvq_gemm_tn(const nvq_qtensor* A, const nvq_qtensor* B, const void* b
     CUtensorMap am, bm;
     GemmArgs* g = new (std::nothrow) GemmArgs;
     if (!g) return NVQ_ERR_CUDA;
-    nvq_status s = gemm_prepare(A, B, &am, &bm, g);
+    nvq_status s = gemm_prepare(A, B, B->rows, &am, &bm, g);
     if (s == NVQ_OK) s = check_c(C, ldc, B->rows, c_fp32);
     if (s == NVQ_OK && bias && !aligned16(bias)) s = NVQ_ERR_ALIGN;
     if (s == NVQ_OK) {
-        g->n_tiles = (int)(B->rows / 128);
+        g->n_tiles = (int)(B->rows / g->block_n);
         g->total_m_tiles = (int)(A->rows / 128);
         g->G = 1;
         g->bias = static_cast<const uint16_t*>(bias);
@@ -467,7 +475,12 @@ nvq_status nvq_grouped_gemm_rows(const nvq_qtensor* A, const nvq_qtensor* B, con
     CUtensorMap am, bm;
     GemmArgs* g = new (std::nothrow) GemmArgs;
     if (!g) return NVQ_ERR_CUDA;
-    nvq_status s = gemm_prepare(A, B, &am, &bm, g);
+    if (!A || !B) {
+        delete g;
+        return NVQ_ERR_NULL;
+    }
+    const int64_t n_out_guess = b_col_groups ? B->rows : n_per_group;
+    nvq_status s = gemm_prepare(A, B, n_out_guess, &am, &bm, g);
     int64_t n_out = 0, klen = 0;
     if (s == NVQ_OK) {
         if (n_per_group <= 0 || n_per_group % 128) s = NVQ_ERR_SHAPE;
@@ -484,7 +497,7 @@ nvq_status nvq_grouped_gemm_rows(const nvq_qtensor* A, const nvq_qtensor* B, con
     if (s == NVQ_OK && nvq_grouped_padded_rows(group_rows, G) != A->rows) s = NVQ_ERR_SHAPE;
     if (s == NVQ_OK) s = check_c(C, ldc, n_out, 0);
     if (s == NVQ_OK) {
-        g->n_tiles = (int)(n_out / 128);
+        g->n_tiles = (int)(n_out / g->block_n);
         g->G = G;
         g->C = C;
         g->ldc = ldc;
@@ -521,11 +534,15 @@ nvq_status nvq_grouped_gemm_wgrad(const nvq_qtensor* A, const nvq_qtensor* B, co
     CUtensorMap am, bm;
     GemmArgs* g = new (std::nothrow) GemmArgs;
     if (!g) return NVQ_ERR_CUDA;
-    nvq_status s = gemm_prepare(A, B, &am, &bm, g);
+    if (!A || !B) {
+        delete g;
+        return NVQ_ERR_NULL;
+    }
+    nvq_status s = gemm_prepare(A, B, B->rows, &am, &bm, g);
     if (s == NVQ_OK && (A->cols != B->cols || nvq_grouped_padded_rows(group_rows, G) != A->cols)) s = NVQ_ERR_SHAPE;
     if (s == NVQ_OK) s = check_c(C, ldc, B->rows, 0);
     if (s == NVQ_OK) {
-        g->n_tiles = (int)(B->rows / 128);
+        g->n_tiles = (int)(B->rows / g->block_n);
         g->G = G;
         g->C = C;
         g->ldc = ldc;

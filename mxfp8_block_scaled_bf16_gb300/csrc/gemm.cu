@@ -8,23 +8,30 @@
 // MXFP8 GEMM (E8M0 1x32 block scales) on direction-specific sub-storages,
 // and the grouped GEMM over experts.
 //
-// Structure (one CTA per 128 x 128 output tile, 6 warps):
-//   warp 0      TMA producer: A/B tiles (128 rows x 128 bytes, 128B swizzle)
-//               with cp.async.bulk.tensor, block scales (whole 512-byte 128x4
-//               tiles of the swizzled scale layout) with cp.async.bulk, into
-//               a ring of smem stages guarded by full/empty mbarriers;
+// Structure: a persistent kernel, one CTA per SM, each CTA walking output
+// tiles of 128 x BN (BN = 256 when the output width allows, else 128) in a
+// static round-robin order (column tiles fastest, so the CTAs in flight share
+// A rows and sweep B from L2).  10 warps:
+//   warp 0      TMA producer: A (128 rows x 128 bytes) and B (BN rows x 128
+//               bytes) tiles with cp.async.bulk.tensor (128B swizzle) and the
+//               matching 512-byte 128x4 block-scale tiles with cp.async.bulk
+//               into a ring of smem stages (full/empty mbarriers);
 //   warp 1      TMEM owner and MMA issuer: per stage copies the scale tiles
-//               smem -> TMEM (tcgen05.cp 32x128b.warpx4, one TMEM column
-//               group per stage so a refill never overwrites scales still in
-//               use) and issues 4 block-scaled MMAs of K = 64 (NVFP4,
-//               kind::mxf4nvf4, scale_vec::4X) or K = 32 (MXFP8,
-//               kind::mxf8f6f4, scale_vec::1X with the scale byte picked by
-//               the scale-factor id), accumulating fp32 in TMEM;
-//   warps 2..5  epilogue: tcgen05.ld of the accumulator (warp w reads TMEM lane
-//               quadrant w % 4), alpha scaling, bias, bf16/fp32 stores.
-// Every mbarrier wait is bounded; on expiry the kernel records
-// NVQ_ERR_TIMEOUT, waits (bounded) for its own copies and MMAs in flight,
-// frees its TMEM and returns.
+//               smem -> TMEM (tcgen05.cp 32x128b.warpx4; each ring stage owns
+//               its TMEM columns so a refill never overwrites scales in use)
+//               and issues 4 block-scaled MMAs (NVFP4: kind::mxf4nvf4
+//               scale_vec::4X, K = 64; MXFP8: kind::mxf8f6f4 scale_vec::1X,
+//               K = 32, the scale byte chosen by the scale-factor id),
+//               accumulating fp32 into one of the TMEM accumulator stages;
+//   warps 2..9  epilogue: warp w reads TMEM lane quadrant w % 4, half
+//               (w - 2) / 4 of the columns; it loads its whole slice, releases
+//               the accumulator to the MMA warp, then scales by alpha, adds
+//               the bias and stores bf16 / fp32 rows while the next tile's
+//               MMAs run.
+// Every mbarrier wait is bounded; a wait that runs out records
+// NVQ_ERR_TIMEOUT and raises a CTA-wide abort flag so all roles leave their
+// loops; the producer then waits (bounded) for its copies in flight and the
+// MMA warp for its tensor-core work before TMEM is freed.
 #include <cuda.h>
 
 #include "nvq_device.cuh"
@@ -35,57 +42,48 @@ namespace nvq {
 namespace gemm {
 
 constexpr int BM = 128;
-constexpr int BN = 128;
-constexpr int kStages = 5;
-constexpr int kTileBytes = 128 * 128;  // one A or B stage: 128 rows x 128 bytes
-constexpr int kThreads = 192;
+constexpr int kTileBytesA = 128 * 128;
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kAccCol = 0;
-constexpr uint32_t kSfCol0 = BN;  // scale ring starts after the accumulator
 
-template <int FMT>
-struct Cfg;
-
-template <>
-struct Cfg<1> {                        // NVFP4
-    static constexpr int kStageK = 256;  // elements per stage (128 bytes of packed E2M1)
-    static constexpr int kMmaK = 64;
-    static constexpr int kAtomsPerStage = 4;  // 128x4 scale tiles (64 elements each) per stage
-    static constexpr int kElemPerAtom = 64;
-    static constexpr uint32_t kSfColsPerStage = 2 * 4 * 4;  // A + B, 4 atoms, 4 columns each
-};
-
-template <>
-struct Cfg<2> {                        // MXFP8
-    static constexpr int kStageK = 128;
-    static constexpr int kMmaK = 32;
-    static constexpr int kAtomsPerStage = 1;  // one 128x4 tile covers 128 elements
-    static constexpr int kElemPerAtom = 128;
-    static constexpr uint32_t kSfColsPerStage = 2 * 4;
-};
-
-template <int FMT>
-struct Smem {
-    static constexpr int kSfBytes = Cfg<FMT>::kAtomsPerStage * 512;
+template <int FMT, int BN>
+struct Cfg {
+    static constexpr int kStageK = FMT == 1 ? 256 : 128;        // elements per stage (128 bytes)
+    static constexpr int kMmaK = FMT == 1 ? 64 : 32;
+    static constexpr int kAtomsK = FMT == 1 ? 4 : 1;            // 128x4 scale tiles along K per stage
+    static constexpr int kElemPerAtom = FMT == 1 ? 64 : 128;
+    static constexpr int kBHalves = BN / 128;
+    static constexpr int kStages = BN == 256 ? 4 : 6;
+    static constexpr int kAccStages = BN == 256 ? 1 : 2;
+    static constexpr int kTileBytesB = BN * 128;
+    static constexpr int kSfaBytes = kAtomsK * 512;
+    static constexpr int kSfbBytes = kAtomsK * 512 * kBHalves;
+    static constexpr uint32_t kSfaCols = 4 * kAtomsK;
+    static constexpr uint32_t kSfbCols = 4 * kAtomsK * kBHalves;
+    static constexpr uint32_t kSfCol0 = BN * kAccStages;
+    static constexpr uint32_t kSfColsPerStage = kSfaCols + kSfbCols;
+    static_assert(kSfCol0 + kStages * kSfColsPerStage <= kTmemCols, "TMEM budget");
+    // shared memory layout (offsets from a 1024-aligned base)
     static constexpr int kA = 0;
-    static constexpr int kB = kA + kStages * kTileBytes;
-    static constexpr int kSfa = kB + kStages * kTileBytes;
-    static constexpr int kSfb = kSfa + kStages * kSfBytes;
-    static constexpr int kBar = kSfb + kStages * kSfBytes;  // full[S], empty[S], tmem_full, mma_done
-    static constexpr int kTmemPtr = kBar + (2 * kStages + 2) * 8;
-    static constexpr int kEnd = kTmemPtr + 16;
-    static constexpr int kAlloc = kEnd + 1024;  // slack for 1024-byte alignment of the base
+    static constexpr int kB = kA + kStages * kTileBytesA;
+    static constexpr int kSfa = kB + kStages * kTileBytesB;
+    static constexpr int kSfb = kSfa + kStages * kSfaBytes;
+    static constexpr int kBar = kSfb + kStages * kSfbBytes;
+    static constexpr int kNumBars = 2 * kStages + 2 * kAccStages + 1;
+    static constexpr int kMisc = kBar + kNumBars * 8;  // tmem address, abort flag
+    static constexpr int kAlloc = kMisc + 16 + 1024;
+    static_assert(kAlloc <= 232448, "shared memory budget");
 };
 
 // Instruction descriptor (kind::mxf4nvf4 / kind::mxf8f6f4 block-scaled):
 // bits 4-5 B scale id, 7-9 A type, 10-12 B type, 15/16 K-major (0),
 // 17-22 N >> 3, 23 scale type (0 UE4M3, 1 UE8M0), 24-28 M >> 4, 29-30 A scale id.
-template <int FMT>
+template <int FMT, int BN>
 __device__ __forceinline__ uint32_t make_idesc(uint32_t sf_id)
 {
     uint32_t d = 0;
-    if (FMT == 1) d |= (1u << 7) | (1u << 10);  // E2M1 x E2M1
-    // FMT == 2: E4M3 = 0 for both operands
+    if (FMT == 1) d |= (1u << 7) | (1u << 10);  // E2M1 x E2M1 (E4M3 = 0 for MXFP8)
     d |= (uint32_t)(BN >> 3) << 17;
     if (FMT == 2) d |= 1u << 23;
     d |= (uint32_t)(BM >> 4) << 24;
@@ -94,51 +92,84 @@ __device__ __forceinline__ uint32_t make_idesc(uint32_t sf_id)
     return d;
 }
 
-__device__ __forceinline__ int find_gemm_group(const GemmArgs& g, int m_tile)
+struct Tile {
+    int g, mt_local, n_tile, a_row, b_row, a_k0, b_k0, k_len, num_kb;
+};
+
+template <int BN, int STAGE_K>
+__device__ __forceinline__ Tile decode(const GemmArgs& a, int t)
 {
-    int lo = 0, hi = g.G - 1;
-    while (lo < hi) {
+    Tile r;
+    const int m_tile = t / a.n_tiles;
+    r.n_tile = t - m_tile * a.n_tiles;
+    int lo = 0, hi = a.G - 1;
+    while (lo < hi) {  // last group whose first tile <= m_tile (empty groups own no tile)
         const int mid = (lo + hi + 1) >> 1;
-        if (g.groups[mid].m_tile0 <= m_tile) lo = mid;
+        if (a.groups[mid].m_tile0 <= m_tile) lo = mid;
         else hi = mid - 1;
     }
-    return lo;
+    const GemmGroup& gr = a.groups[lo];
+    r.g = lo;
+    r.mt_local = m_tile - gr.m_tile0;
+    r.a_row = gr.a_row0 + r.mt_local * BM;
+    r.b_row = gr.b_row0 + r.n_tile * BN;
+    r.a_k0 = gr.a_k0;
+    r.b_k0 = gr.b_k0;
+    r.k_len = gr.k_len;
+    r.num_kb = (gr.k_len + STAGE_K - 1) / STAGE_K;
+    return r;
 }
 
-template <int FMT>
+// Bounded wait that also gives up when another role has aborted the CTA.
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, int* status, volatile int* abort_flag)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 0;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 63) == 63) {
+            if (*abort_flag) return false;
+            if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                record_error(status, kErrTimeout);
+                *abort_flag = 1;
+                return false;
+            }
+        }
+    }
+}
+
+template <int FMT, int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap a_map, const __grid_constant__ CUtensorMap b_map,
                 const __grid_constant__ GemmArgs args)
 {
-    using C = Cfg<FMT>;
-    using L = Smem<FMT>;
+    using C = Cfg<FMT, BN>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBar);
-    uint64_t* empty = full + kStages;
-    uint64_t* tmem_full = empty + kStages;
-    uint64_t* mma_done = tmem_full + 1;
-    uint32_t* tmem_ptr = reinterpret_cast<uint32_t*>(smem + L::kTmemPtr);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kBar);
+    uint64_t* empty = full + C::kStages;
+    uint64_t* acc_full = empty + C::kStages;
+    uint64_t* acc_empty = acc_full + C::kAccStages;
+    uint64_t* mma_done = acc_empty + C::kAccStages;
+    uint32_t* tmem_ptr = reinterpret_cast<uint32_t*>(smem + C::kMisc);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kMisc + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int tile = blockIdx.x;
-    const int m_tile = tile / args.n_tiles, n_tile = tile % args.n_tiles;
-    const int g = find_gemm_group(args, m_tile);
-    const GemmGroup& gr = args.groups[g];
-    const int mt_local = m_tile - gr.m_tile0;
-    const int a_row = gr.a_row0 + mt_local * BM;
-    const int b_row = gr.b_row0 + n_tile * BN;
-    const int num_kb = (gr.k_len + C::kStageK - 1) / C::kStageK;
+    const int total = args.total_m_tiles * args.n_tiles;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < C::kStages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
-        mbar_init(tmem_full, 1);
+        for (int s = 0; s < C::kAccStages; ++s) {
+            mbar_init(&acc_full[s], 1);
+            mbar_init(&acc_empty[s], kEpiWarps);
+        }
         mbar_init(mma_done, 1);
+        *abort_flag = 0;
         fence_mbarrier_init();
-        if (num_kb > 0) {
+        if (args.any_k) {
             tma_prefetch_desc(&a_map);
             tma_prefetch_desc(&b_map);
         }
@@ -153,130 +184,161 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem_base = *tmem_ptr;
 
     if (warp == 0) {
-        // ---------------- TMA producer
-        if (lane == 0 && num_kb > 0) {
-            int issued = 0;
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            uint32_t it = 0;
             bool ok = true;
-            for (int kb = 0; kb < num_kb && ok; ++kb) {
-                const int s = kb % kStages;
-                const uint32_t round = kb / kStages;
-                if (!mbar_wait(&empty[s], (round & 1) ^ 1, args.status)) { ok = false; break; }
-                const int kel_a = gr.a_k0 + kb * C::kStageK;  // first contraction element of the stage
-                const int kel_b = gr.b_k0 + kb * C::kStageK;
-                const int left = gr.k_len - kb * C::kStageK;
-                const int atoms = min(C::kAtomsPerStage, (left + C::kElemPerAtom - 1) / C::kElemPerAtom);
-                const uint32_t sf_bytes = (uint32_t)atoms * 512u;
-                mbar_arrive_expect_tx(&full[s], 2u * kTileBytes + 2u * sf_bytes);
-                tma_load_2d(smem + L::kA + s * kTileBytes, &a_map, &full[s], FMT == 1 ? kel_a / 2 : kel_a, a_row);
-                tma_load_2d(smem + L::kB + s * kTileBytes, &b_map, &full[s], FMT == 1 ? kel_b / 2 : kel_b, b_row);
-                const uint8_t* sfa = args.a_scale +
-                    ((int64_t)(a_row / 128) * args.a_scale_ctiles + kel_a / C::kElemPerAtom) * 512;
-                const uint8_t* sfb = args.b_scale +
-                    ((int64_t)(b_row / 128) * args.b_scale_ctiles + kel_b / C::kElemPerAtom) * 512;
-                bulk_load(smem + L::kSfa + s * L::kSfBytes, sfa, sf_bytes, &full[s]);
-                bulk_load(smem + L::kSfb + s * L::kSfBytes, sfb, sf_bytes, &full[s]);
-                ++issued;
+            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+                const Tile tl = decode<BN, C::kStageK>(args, t);
+                for (int kb = 0; kb < tl.num_kb; ++kb, ++it) {
+                    const int s = it % C::kStages;
+                    if (!wait_or_abort(&empty[s], ((it / C::kStages) & 1) ^ 1, args.status, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    const int ka = tl.a_k0 + kb * C::kStageK, kbb = tl.b_k0 + kb * C::kStageK;
+                    const int left = tl.k_len - kb * C::kStageK;
+                    const int atoms = min(C::kAtomsK, (left + C::kElemPerAtom - 1) / C::kElemPerAtom);
+                    const uint32_t sf_bytes = (uint32_t)atoms * 512u;
+                    mbar_arrive_expect_tx(&full[s], (uint32_t)(kTileBytesA + C::kTileBytesB) +
+                                                        sf_bytes * (1 + C::kBHalves));
+                    tma_load_2d(smem + C::kA + s * kTileBytesA, &a_map, &full[s], FMT == 1 ? ka / 2 : ka, tl.a_row);
+                    tma_load_2d(smem + C::kB + s * C::kTileBytesB, &b_map, &full[s], FMT == 1 ? kbb / 2 : kbb, tl.b_row);
+                    bulk_load(smem + C::kSfa + s * C::kSfaBytes,
+                              args.a_scale + ((int64_t)(tl.a_row / 128) * args.a_scale_ctiles + ka / C::kElemPerAtom) * 512,
+                              sf_bytes, &full[s]);
+#pragma unroll
+                    for (int h = 0; h < C::kBHalves; ++h)
+                        bulk_load(smem + C::kSfb + s * C::kSfbBytes + h * C::kAtomsK * 512,
+                                  args.b_scale +
+                                      ((int64_t)(tl.b_row / 128 + h) * args.b_scale_ctiles + kbb / C::kElemPerAtom) * 512,
+                                  sf_bytes, &full[s]);
+                }
             }
-            // Drain: wait (bounded) for the copies this thread issued last in
-            // each stage, so none lands in smem after the CTA exits.
-            for (int i = 0; i < min(issued, kStages); ++i) {
-                const int kb = issued - 1 - i;
-                mbar_wait(&full[kb % kStages], (uint32_t)((kb / kStages) & 1), args.status);
+            // drain: the last copy issued into each stage has landed before exit
+            const uint32_t n = it < (uint32_t)C::kStages ? it : (uint32_t)C::kStages;
+            for (uint32_t i = 0; i < n; ++i) {
+                const uint32_t k = it - 1 - i;
+                mbar_wait(&full[k % C::kStages], (k / C::kStages) & 1, args.status);
             }
         }
     } else if (warp == 1) {
-        // ---------------- MMA issuer
+        // ------------------------------------------------ MMA issuer
         if (lane == 0) {
-            const uint32_t d_tmem = tmem_base + kAccCol;
-            for (int kb = 0; kb < num_kb; ++kb) {
-                const int s = kb % kStages;
-                if (!mbar_wait(&full[s], (uint32_t)((kb / kStages) & 1), args.status)) break;
+            uint32_t it = 0, tl_i = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++tl_i) {
+                const Tile tl = decode<BN, C::kStageK>(args, t);
+                const int as = tl_i % C::kAccStages;
+                if (!wait_or_abort(&acc_empty[as], ((tl_i / C::kAccStages) & 1) ^ 1, args.status, abort_flag)) break;
                 tc_fence_after();
-                const int left = gr.k_len - kb * C::kStageK;
-                const int n_mma = min(C::kStageK, left) / C::kMmaK;
-                const int atoms = (min(C::kStageK, left) + C::kElemPerAtom - 1) / C::kElemPerAtom;
-                const uint32_t sf_col = tmem_base + kSfCol0 + (uint32_t)s * C::kSfColsPerStage;
-                const uint32_t sfa_col = sf_col;
-                const uint32_t sfb_col = sf_col + C::kSfColsPerStage / 2;
-                const uint32_t sfa_smem = smem_u32(smem + L::kSfa + s * L::kSfBytes);
-                const uint32_t sfb_smem = smem_u32(smem + L::kSfb + s * L::kSfBytes);
-                for (int j = 0; j < atoms; ++j) {
-                    tc_cp_32x128b_warpx4(sfa_col + 4 * j, smem_desc(sfa_smem + 512 * j, 16, 128, kSwizzleNone));
-                    tc_cp_32x128b_warpx4(sfb_col + 4 * j, smem_desc(sfb_smem + 512 * j, 16, 128, kSwizzleNone));
-                }
-                const uint32_t a_smem = smem_u32(smem + L::kA + s * kTileBytes);
-                const uint32_t b_smem = smem_u32(smem + L::kB + s * kTileBytes);
-                for (int j = 0; j < n_mma; ++j) {
-                    const uint64_t ad = smem_desc(a_smem + 32 * j, 16, 1024, kSwizzle128B);
-                    const uint64_t bd = smem_desc(b_smem + 32 * j, 16, 1024, kSwizzle128B);
-                    const uint32_t acc = (kb > 0 || j > 0) ? 1u : 0u;
-                    if constexpr (FMT == 1) {
-                        tc_mma_nvf4(d_tmem, ad, bd, make_idesc<1>(0), sfa_col + 4 * j, sfb_col + 4 * j, acc);
-                    } else {
-                        tc_mma_mxf8(d_tmem, ad, bd, make_idesc<2>((uint32_t)j), sfa_col, sfb_col, acc);
+                const uint32_t d_tmem = tmem_base + (uint32_t)(as * BN);
+                for (int kb = 0; kb < tl.num_kb; ++kb, ++it) {
+                    const int s = it % C::kStages;
+                    if (!wait_or_abort(&full[s], (it / C::kStages) & 1, args.status, abort_flag)) {
+                        ok = false;
+                        break;
                     }
+                    tc_fence_after();
+                    const int left = tl.k_len - kb * C::kStageK;
+                    const int n_mma = min(C::kStageK, left) / C::kMmaK;
+                    const int atoms = (min(C::kStageK, left) + C::kElemPerAtom - 1) / C::kElemPerAtom;
+                    const uint32_t sfa_col = tmem_base + C::kSfCol0 + (uint32_t)s * C::kSfColsPerStage;
+                    const uint32_t sfb_col = sfa_col + C::kSfaCols;
+                    const uint32_t sfa_smem = smem_u32(smem + C::kSfa + s * C::kSfaBytes);
+                    const uint32_t sfb_smem = smem_u32(smem + C::kSfb + s * C::kSfbBytes);
+                    for (int j = 0; j < atoms; ++j) {
+                        tc_cp_32x128b_warpx4(sfa_col + 4 * j, smem_desc(sfa_smem + 512 * j, 16, 128, kSwizzleNone));
+#pragma unroll
+                        for (int h = 0; h < C::kBHalves; ++h)
+                            tc_cp_32x128b_warpx4(sfb_col + 4 * (C::kBHalves * j + h),
+                                                 smem_desc(sfb_smem + 512 * (h * C::kAtomsK + j), 16, 128, kSwizzleNone));
+                    }
+                    const uint32_t a_smem = smem_u32(smem + C::kA + s * kTileBytesA);
+                    const uint32_t b_smem = smem_u32(smem + C::kB + s * C::kTileBytesB);
+                    for (int j = 0; j < n_mma; ++j) {
+                        const uint64_t ad = smem_desc(a_smem + 32 * j, 16, 1024, kSwizzle128B);
+                        const uint64_t bd = smem_desc(b_smem + 32 * j, 16, 1024, kSwizzle128B);
+                        const uint32_t acc = (kb > 0 || j > 0) ? 1u : 0u;
+                        if constexpr (FMT == 1)
+                            tc_mma_nvf4(d_tmem, ad, bd, make_idesc<1, BN>(0), sfa_col + 4 * j,
+                                        sfb_col + 4 * C::kBHalves * j, acc);
+                        else
+                            tc_mma_mxf8(d_tmem, ad, bd, make_idesc<2, BN>((uint32_t)j), sfa_col, sfb_col, acc);
+                    }
+                    tc_commit(&empty[s]);
                 }
-                tc_commit(&empty[s]);
+                tc_commit(&acc_full[as]);
             }
-            tc_commit(tmem_full);
-            // all of this thread's tensor-core work done before TMEM is freed
+            // all of this thread's tensor-core work has finished before TMEM is freed
             tc_commit(mma_done);
             mbar_wait(mma_done, 0, args.status);
         }
     } else {
-        // ---------------- epilogue (warps 2..5)
+        // ------------------------------------------------ epilogue (warps 2..9)
+        constexpr int kCols = BN / 2;       // columns per warp
+        constexpr int kChunks = kCols / 32;
         const int quad = warp & 3;
-        const int r = quad * 32 + lane;  // row within the tile = TMEM lane
-        float alpha = 1.0f;
-        if (FMT == 1) {
-            const float ga = __fdiv_rn(args.a_amax[gr.amax_idx], 2688.0f);
-            const float gb = __fdiv_rn(args.b_amax[gr.amax_idx], 2688.0f);
-            alpha = __fmul_rn(ga, gb);
-        }
-        bool have_acc = num_kb > 0;
-        if (have_acc) {
-            have_acc = mbar_wait(tmem_full, 0, args.status);
+        const int half = (warp - 2) >> 2;
+        const int r = quad * 32 + lane;     // tile row = TMEM lane
+        uint32_t tl_i = 0;
+        for (int t = blockIdx.x; t < total; t += gridDim.x, ++tl_i) {
+            const Tile tl = decode<BN, C::kStageK>(args, t);
+            const GemmGroup& gr = args.groups[tl.g];
+            const int as = tl_i % C::kAccStages;
+            if (!wait_or_abort(&acc_full[as], (tl_i / C::kAccStages) & 1, args.status, abort_flag)) break;
             tc_fence_after();
-        }
-        const int out_row = mt_local * BM + r;
-        const bool row_ok = out_row < gr.rows_valid;
-        const int col0 = n_tile * BN;
-        for (int c = 0; c < BN / 32; ++c) {
-            uint32_t v[32];
-            if (have_acc) {
-                tmem_ld_32x32b_x32(tmem_base + kAccCol + ((uint32_t)(quad * 32) << 16) + (uint32_t)(c * 32), v);
+            uint32_t v[kCols];
+            if (tl.num_kb > 0) {
+                const uint32_t taddr = tmem_base + (uint32_t)(as * BN + half * kCols) + ((uint32_t)(quad * 32) << 16);
+#pragma unroll
+                for (int c = 0; c < kChunks; ++c) {
+                    uint32_t (&vc)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[c * 32]);
+                    tmem_ld_32x32b_x32(taddr + (uint32_t)(c * 32), vc);
+                }
                 tmem_ld_wait();
             } else {
 #pragma unroll
-                for (int i = 0; i < 32; ++i) v[i] = 0u;
+                for (int i = 0; i < kCols; ++i) v[i] = 0u;  // empty contraction: zero
             }
-            if (!row_ok) continue;
-            float f[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                float y = __fmul_rn(alpha, __uint_as_float(v[i]));
-                if (args.bias) y = __fadd_rn(y, __uint_as_float((uint32_t)args.bias[col0 + c * 32 + i] << 16));
-                f[i] = y;
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[as]);
+
+            const int out_row = tl.mt_local * BM + r;
+            if (out_row >= gr.rows_valid) continue;
+            float alpha = 1.0f;
+            if (FMT == 1) {
+                const float ga = __fdiv_rn(args.a_amax[gr.amax_idx], 2688.0f);
+                const float gb = __fdiv_rn(args.b_amax[gr.amax_idx], 2688.0f);
+                alpha = __fmul_rn(ga, gb);
             }
-            if (args.c_fp32) {
-                float* dst = reinterpret_cast<float*>(args.C) + gr.c_off + (int64_t)out_row * args.ldc + col0 + c * 32;
+            const int col0 = tl.n_tile * BN + half * kCols;
+            const int64_t rowoff = gr.c_off + (int64_t)out_row * args.ldc + col0;
 #pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    reinterpret_cast<float4*>(dst)[i] = make_float4(f[4 * i], f[4 * i + 1], f[4 * i + 2], f[4 * i + 3]);
-            } else {
-                uint16_t* dst = reinterpret_cast<uint16_t*>(args.C) + gr.c_off + (int64_t)out_row * args.ldc + col0 + c * 32;
+            for (int c = 0; c < kChunks; ++c) {
+                float f[32];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    uint4 q;
-                    __nv_bfloat162 p0 = __floats2bfloat162_rn(f[8 * i + 0], f[8 * i + 1]);
-                    __nv_bfloat162 p1 = __floats2bfloat162_rn(f[8 * i + 2], f[8 * i + 3]);
-                    __nv_bfloat162 p2 = __floats2bfloat162_rn(f[8 * i + 4], f[8 * i + 5]);
-                    __nv_bfloat162 p3 = __floats2bfloat162_rn(f[8 * i + 6], f[8 * i + 7]);
-                    q.x = *reinterpret_cast<uint32_t*>(&p0);
-                    q.y = *reinterpret_cast<uint32_t*>(&p1);
-                    q.z = *reinterpret_cast<uint32_t*>(&p2);
-                    q.w = *reinterpret_cast<uint32_t*>(&p3);
-                    reinterpret_cast<uint4*>(dst)[i] = q;
+                for (int i = 0; i < 32; ++i) {
+                    float y = __fmul_rn(alpha, __uint_as_float(v[c * 32 + i]));
+                    if (args.bias) y = __fadd_rn(y, __uint_as_float((uint32_t)args.bias[col0 + c * 32 + i] << 16));
+                    f[i] = y;
+                }
+                if (args.c_fp32) {
+                    float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(args.C) + rowoff + c * 32);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) dst[i] = make_float4(f[4 * i], f[4 * i + 1], f[4 * i + 2], f[4 * i + 3]);
+                } else {
+                    uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(args.C) + rowoff + c * 32);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        __nv_bfloat162 p0 = __floats2bfloat162_rn(f[8 * i + 0], f[8 * i + 1]);
+                        __nv_bfloat162 p1 = __floats2bfloat162_rn(f[8 * i + 2], f[8 * i + 3]);
+                        __nv_bfloat162 p2 = __floats2bfloat162_rn(f[8 * i + 4], f[8 * i + 5]);
+                        __nv_bfloat162 p3 = __floats2bfloat162_rn(f[8 * i + 6], f[8 * i + 7]);
+                        dst[i] = make_uint4(*reinterpret_cast<uint32_t*>(&p0), *reinterpret_cast<uint32_t*>(&p1),
+                                            *reinterpret_cast<uint32_t*>(&p2), *reinterpret_cast<uint32_t*>(&p3));
+                    }
                 }
             }
         }
@@ -290,27 +352,45 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+template <int FMT, int BN>
+cudaError_t set_smem()
+{
+    return cudaFuncSetAttribute(gemm_kernel<FMT, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<FMT, BN>::kAlloc);
+}
+
+template <int FMT, int BN>
+void launch(const CUtensorMap& am, const CUtensorMap& bm, const GemmArgs& g, int grid, cudaStream_t s)
+{
+    gemm_kernel<FMT, BN><<<grid, kThreads, Cfg<FMT, BN>::kAlloc, s>>>(am, bm, g);
+}
+
 }  // namespace gemm
 
 cudaError_t init_gemm_attributes()
 {
-    cudaError_t e = cudaFuncSetAttribute(gemm::gemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         gemm::Smem<1>::kAlloc);
-    if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(gemm::gemm_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                gemm::Smem<2>::kAlloc);
+    cudaError_t e = gemm::set_smem<1, 128>();
+    if (e == cudaSuccess) e = gemm::set_smem<1, 256>();
+    if (e == cudaSuccess) e = gemm::set_smem<2, 128>();
+    if (e == cudaSuccess) e = gemm::set_smem<2, 256>();
+    return e;
 }
 
-cudaError_t launch_gemm(const void* a_map, const void* b_map, const GemmArgs& g, cudaStream_t s)
+int gemm_block_n(int64_t n_out) { return n_out % 256 == 0 ? 256 : 128; }
+
+cudaError_t launch_gemm(const void* a_map, const void* b_map, const GemmArgs& g, int num_sms, cudaStream_t s)
 {
     const int tiles = g.total_m_tiles * g.n_tiles;
     if (tiles == 0) return cudaSuccess;
+    const int grid = tiles < num_sms ? tiles : num_sms;
     const CUtensorMap& am = *reinterpret_cast<const CUtensorMap*>(a_map);
     const CUtensorMap& bm = *reinterpret_cast<const CUtensorMap*>(b_map);
-    if (g.fmt == 1)
-        gemm::gemm_kernel<1><<<tiles, gemm::kThreads, gemm::Smem<1>::kAlloc, s>>>(am, bm, g);
-    else
-        gemm::gemm_kernel<2><<<tiles, gemm::kThreads, gemm::Smem<2>::kAlloc, s>>>(am, bm, g);
+    if (g.fmt == 1) {
+        if (g.block_n == 256) gemm::launch<1, 256>(am, bm, g, grid, s);
+        else gemm::launch<1, 128>(am, bm, g, grid, s);
+    } else {
+        if (g.block_n == 256) gemm::launch<2, 256>(am, bm, g, grid, s);
+        else gemm::launch<2, 128>(am, bm, g, grid, s);
+    }
     return cudaGetLastError();
 }
 

@@ -68,6 +68,8 @@ struct GemmGroup {
 
 struct GemmArgs {
     int fmt;               // 1 NVFP4, 2 MXFP8
+    int block_n;           // output tile width BN (128 or 256)
+    int any_k;             // some group has a nonzero contraction (tensor maps valid)
     int n_tiles;           // output column tiles (N / BN)
     int total_m_tiles;     // sum of m_tiles
     int G;
@@ -85,8 +87,12 @@ struct GemmArgs {
     GemmGroup groups[kMaxGroups];
 };
 
-// A_map / B_map: CUtensorMap (128-byte aligned, 128 bytes each).
-cudaError_t launch_gemm(const void* a_map, const void* b_map, const GemmArgs& g, cudaStream_t s);
+// Output tile width for an output of n_out columns (a multiple of 128).
+int gemm_block_n(int64_t n_out);
+
+// A_map / B_map: CUtensorMap (boxes 128 x 128 bytes for A, block_n x 128 for B).
+// Persistent launch: min(tiles, num_sms) CTAs.
+cudaError_t launch_gemm(const void* a_map, const void* b_map, const GemmArgs& g, int num_sms, cudaStream_t s);
 
 cudaError_t init_gemm_attributes();
 
