@@ -183,8 +183,13 @@ nvq_status quantize_impl(const void* x, int64_t M, int64_t K, int64_t ld, const 
     const bool any_nv = row_fmt == NVQ_FMT_NVFP4 || col_fmt == NVQ_FMT_NVFP4;
     if (sr && any_nv) {
         const uint64_t s = (uint64_t)sr->seed;
-        a.sr_key0 = (uint32_t)s;
-        a.sr_key1 = (uint32_t)(s >> 32);
+        uint32_t k0 = (uint32_t)s, k1 = (uint32_t)(s >> 32);
+        for (int r = 0; r < 10; ++r) {  // Philox4x32-10 key schedule (Weyl increments)
+            a.sr_round_key[2 * r] = k0;
+            a.sr_round_key[2 * r + 1] = k1;
+            k0 += 0x9E3779B9u;
+            k1 += 0xBB67AE85u;
+        }
         a.sr_offset = sr->offset;
     }
     if (!do_row && !do_col) return NVQ_OK;

@@ -286,7 +286,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const Tile tl = decode<BN, C::kStageK>(args, t);
             const GemmGroup& gr = args.groups[tl.g];
             const int as = tl_i % C::kAccStages;
-            if (!wait_or_abort(&acc_full[as], (tl_i / C::kAccStages) & 1, args.status, abort_flag)) break;
+            // one lane polls, the warp reconverges before the .sync.aligned TMEM loads
+            int ok = 1;
+            if (lane == 0) ok = wait_or_abort(&acc_full[as], (tl_i / C::kAccStages) & 1, args.status, abort_flag);
+            ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+            if (!ok) break;
             tc_fence_after();
             uint32_t v[kCols];
             if (tl.num_kb > 0) {

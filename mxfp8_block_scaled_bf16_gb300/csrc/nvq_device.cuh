@@ -310,6 +310,24 @@ __device__ __forceinline__ Philox4 philox4x32_10(uint32_t c0, uint32_t c1, uint3
     return {c0, c1, c2, c3};
 }
 
+// Same generator with the key schedule precomputed: rk[2r], rk[2r+1] are the
+// key words of round r.
+__device__ __forceinline__ Philox4 philox4x32_10_rk(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3,
+                                                    const uint32_t (&rk)[20])
+{
+#pragma unroll
+    for (int round = 0; round < 10; ++round) {
+        const uint32_t lo0 = 0xD2511F53u * c0, hi0 = __umulhi(0xD2511F53u, c0);
+        const uint32_t lo1 = 0xCD9E8D57u * c2, hi1 = __umulhi(0xCD9E8D57u, c2);
+        const uint32_t n0 = hi1 ^ c1 ^ rk[2 * round], n2 = hi0 ^ c3 ^ rk[2 * round + 1];
+        c0 = n0;
+        c1 = lo1;
+        c2 = n2;
+        c3 = lo0;
+    }
+    return {c0, c1, c2, c3};
+}
+
 // 16-bit random field f (0..7) of a Philox block.
 __device__ __forceinline__ uint32_t philox_field(const Philox4& p, int f)
 {

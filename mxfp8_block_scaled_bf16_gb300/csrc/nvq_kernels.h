@@ -43,7 +43,8 @@ struct QuantArgs {
     float* amax_rht_out;
     // RHT and SR
     uint32_t rht_sign_mask;  // bit i set: sign[i] == -1
-    uint32_t sr_key0, sr_key1, sr_offset;
+    uint32_t sr_offset;
+    uint32_t sr_round_key[20];  // Philox key schedule: (k0 + r*W0, k1 + r*W1), r = 0..9
     int* status;  // device status word
 };
 

@@ -83,12 +83,24 @@ __device__ __forceinline__ void column16(const ThreadTile& t, int j, float (&u)[
     }
 }
 
-// T(u) = 1/4 H16 (s .* u): sign flip, butterflies with spans 1, 2, 4, 8, scale.
-__device__ __forceinline__ void rht16(float (&u)[16], uint32_t sign_mask)
+// s .* u for the thread's 16 rows: row i of the tile is negated (sign bits of
+// both bf16 halves of every word flipped) where sign[i] == -1.
+__device__ __forceinline__ void flip_rows(ThreadTile& t, uint32_t sign_mask)
 {
 #pragma unroll
-    for (int i = 0; i < 16; ++i)
-        if (sign_mask & (1u << i)) u[i] = -u[i];
+    for (int i = 0; i < 16; ++i) {
+        const uint32_t m = ((sign_mask >> i) & 1u) ? 0x80008000u : 0u;
+        t.w[i].x ^= m;
+        t.w[i].y ^= m;
+        t.w[i].z ^= m;
+        t.w[i].w ^= m;
+    }
+}
+
+// T(u) = 1/4 H16 u for an already sign-flipped u: butterflies with spans
+// 1, 2, 4, 8 ((a, b) -> (a + b, a - b)), then the exact 1/4.
+__device__ __forceinline__ void hadamard16(float (&u)[16])
+{
 #pragma unroll
     for (int h = 1; h < 16; h <<= 1) {
 #pragma unroll
@@ -117,7 +129,7 @@ __device__ __forceinline__ float warp_max(float v)
 }
 
 // ------------------------------------------------------------------ amax pass
-__global__ void __launch_bounds__(kThreads) amax_kernel(QuantArgs a)
+__global__ void __launch_bounds__(kThreads, 2) amax_kernel(QuantArgs a)
 {
     const int64_t tile_row = blockIdx.y;
     const int g = find_group(a.groups, tile_row);
@@ -137,11 +149,12 @@ __global__ void __launch_bounds__(kThreads) amax_kernel(QuantArgs a)
         for (int j = 0; j < 8; ++j) m_plain = fmaxf(m_plain, fabsf(v[j]));
     }
     if (a.amax_rht_out) {
+        flip_rows(t, a.rht_sign_mask);
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             float u[16];
             column16(t, j, u);
-            rht16(u, a.rht_sign_mask);
+            hadamard16(u);
 #pragma unroll
             for (int i = 0; i < 16; ++i) m_rht = fmaxf(m_rht, fabsf(u[i]));
         }
@@ -209,8 +222,8 @@ __device__ __forceinline__ uint32_t nvfp4_encode8(const float (&v)[8], float e, 
     for (int j = 0; j < 8; ++j) s[j] = __fmul_rn(v[j], e);
     if constexpr (SR) {
         const uint64_t blk = L0 >> 3;
-        const Philox4 p = philox4x32_10((uint32_t)blk, (uint32_t)(blk >> 32), (uint32_t)dir,
-                                        a.sr_offset, a.sr_key0, a.sr_key1);
+        const Philox4 p = philox4x32_10_rk((uint32_t)blk, (uint32_t)(blk >> 32), (uint32_t)dir, a.sr_offset,
+                                           a.sr_round_key);
 #pragma unroll
         for (int j = 0; j < 8; ++j) s[j] = e2m1_sr_value(s[j], philox_field(p, j));
     }
@@ -239,15 +252,21 @@ __device__ __forceinline__ float exp2_neg(int e)
 }
 
 // ------------------------------------------------------------------ fused quantize
-// Shared staging: transposed codes and both scale tiles.
+// Shared staging: transposed codes and both scale tiles.  Output row kk of
+// the transposed codes holds 64 (NVFP4) or 128 (MXFP8) bytes; its 8- or
+// 16-byte chunks are XOR-swizzled by (kk >> 3) & 7 so the lanes of a warp
+// (8 output rows apart) hit different banks.
 struct QuantSmem {
-    uint8_t col_codes[kTileCols][kTileRows + 16];  // per output row k: up to 128 B (MXFP8) + pad
+    uint8_t col_codes[kTileCols * kTileRows];
     uint8_t row_scales[2048];                      // 128 rows x up to 16 scale cols
     uint8_t col_scales[2][1024];                   // 2 x (128 k-rows x up to 8 scale cols)
 };
 
+__device__ __forceinline__ int col_chunk_nv(int kk, int ch8) { return kk * 64 + ((ch8 ^ ((kk >> 3) & 7)) << 3); }
+__device__ __forceinline__ int col_chunk_mx(int kk, int ch16) { return kk * 128 + ((ch16 ^ ((kk >> 3) & 7)) << 4); }
+
 template <int ROW_FMT, int COL_FMT, bool RHT, bool SR>
-__global__ void __launch_bounds__(kThreads) quantize_kernel(QuantArgs a)
+__global__ void __launch_bounds__(kThreads, 2) quantize_kernel(QuantArgs a)
 {
     __shared__ __align__(16) QuantSmem sm;
     const int64_t tile_row = blockIdx.y, tile_col = blockIdx.x;
@@ -318,11 +337,12 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(QuantArgs a)
     // ---------------- columnwise direction (output row = column k, contraction = padded row p)
     if constexpr (COL_FMT == 1) {  // NVFP4: the thread's 16 rows form one block per column
         const Nvfp4Scale ts = nvfp4_tensor_scale(a.col_amax[g]);
+        if constexpr (RHT) flip_rows(t, a.rht_sign_mask);  // the rowwise pass is done with t
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             float u[16];
             column16(t, j, u);
-            if constexpr (RHT) rht16(u, a.rht_sign_mask);
+            if constexpr (RHT) hadamard16(u);
             float b = 0.0f;
 #pragma unroll
             for (int i = 0; i < 16; ++i) b = fmaxf(b, fabsf(u[i]));
@@ -335,7 +355,7 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(QuantArgs a)
             for (int i = 0; i < 8; ++i) { h0[i] = u[i]; h1[i] = u[i + 8]; }
             const uint32_t c0 = nvfp4_encode8<SR>(h0, e, Lbase, 1, a);
             const uint32_t c1 = nvfp4_encode8<SR>(h1, e, Lbase + 8, 1, a);
-            *reinterpret_cast<uint2*>(&sm.col_codes[c_loc + j][r_loc / 2]) = make_uint2(c0, c1);
+            *reinterpret_cast<uint2*>(&sm.col_codes[col_chunk_nv(c_loc + j, r_loc / 16)]) = make_uint2(c0, c1);
             const int kk = c_loc + j;      // output row within CTA (0..255)
             const int c = r_loc / 16;      // scale column within CTA (0..7)
             sm.col_scales[kk >> 7][(c >> 2) * 512 + (kk & 31) * 16 + ((kk >> 5) & 3) * 4 + (c & 3)] =
@@ -357,7 +377,7 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(QuantArgs a)
             q.y = e4m3x4_rn(__fmul_rn(u[4], sc), __fmul_rn(u[5], sc), __fmul_rn(u[6], sc), __fmul_rn(u[7], sc));
             q.z = e4m3x4_rn(__fmul_rn(u[8], sc), __fmul_rn(u[9], sc), __fmul_rn(u[10], sc), __fmul_rn(u[11], sc));
             q.w = e4m3x4_rn(__fmul_rn(u[12], sc), __fmul_rn(u[13], sc), __fmul_rn(u[14], sc), __fmul_rn(u[15], sc));
-            *reinterpret_cast<uint4*>(&sm.col_codes[c_loc + j][r_loc]) = q;
+            *reinterpret_cast<uint4*>(&sm.col_codes[col_chunk_mx(c_loc + j, r_loc / 16)]) = q;
             if ((lane >> 4) == 0) {
                 const int kk = c_loc + j;
                 const int c = r_loc / 32;  // 0..3
@@ -383,17 +403,22 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(QuantArgs a)
         }
     }
     if constexpr (COL_FMT != 0) {
-        constexpr int bytes_per_k = COL_FMT == 1 ? kTileRows / 2 : kTileRows;  // codes per output row
         const int64_t row_bytes = COL_FMT == 1 ? a.col_cols_store / 2 : a.col_cols_store;
         const int64_t byte0 = COL_FMT == 1 ? p_tile0 / 2 : p_tile0;
-        constexpr int chunks = bytes_per_k / 8;  // 8-byte chunks per output row
-        for (int i = threadIdx.x; i < kTileCols * chunks; i += kThreads) {
-            const int kk = i / chunks, ch = i % chunks;
+        for (int i = threadIdx.x; i < kTileCols * 8; i += kThreads) {
+            const int kk = i >> 3, ch = i & 7;  // 8 chunks per output row
             const int64_t k = tile_col * kTileCols + kk;
-            const int64_t off = byte0 + ch * 8;
-            if (k < a.K && off < row_bytes)
-                *reinterpret_cast<uint2*>(a.col_data + k * row_bytes + off) =
-                    *reinterpret_cast<const uint2*>(&sm.col_codes[kk][ch * 8]);
+            if (COL_FMT == 1) {
+                const int64_t off = byte0 + ch * 8;
+                if (k < a.K && off < row_bytes)
+                    *reinterpret_cast<uint2*>(a.col_data + k * row_bytes + off) =
+                        *reinterpret_cast<const uint2*>(&sm.col_codes[col_chunk_nv(kk, ch)]);
+            } else {
+                const int64_t off = byte0 + ch * 16;
+                if (k < a.K && off < row_bytes)
+                    *reinterpret_cast<uint4*>(a.col_data + k * row_bytes + off) =
+                        *reinterpret_cast<const uint4*>(&sm.col_codes[col_chunk_mx(kk, ch)]);
+            }
         }
         // scales: output rows k (two 128-row tile-rows), scale columns p/16 (NVFP4, 2 tiles) or p/32 (1 tile)
         constexpr int nct = COL_FMT == 1 ? 2 : 1;

@@ -1,0 +1,140 @@
+"""Parity at the benchmark's full sizes, in the launch configuration bench.py
+times.
+
+* Llama-3-8B MLP up-projection (x[16384,4096], W[14336,4096], dy[16384,14336],
+  SR seed 1234, RHT signs seed 7): every quantized operand of the step is
+  compared bit for bit with the oracle over the whole tensor; the three GEMM
+  outputs on sampled entries (random positions plus one full row and one full
+  column) that the oracle computes one by one from its own operands.
+* MoE grouped linear (64 experts 4096->1536, 65536 Zipf(1.1) tokens): operands
+  and outputs of a spread of experts (the smallest, the largest, empty ones)
+  against the oracle.
+
+Pages: "Add an NVFP4 quantization converter" (Llama-3-8B run, NVFP4Linear) and
+"Hybrid quantization" (GroupedLinear with NVFP4 forward / MXFP8 backward)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import mxfp8_block_scaled_bf16_gb300 as nvq
+from mxfp8_block_scaled_bf16_gb300 import inputs
+
+from gpu_util import assert_codes_equal, assert_scales_equal, bits, bf16_from_bits, qt_codes, qt_scales
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    import __graft_entry__
+    __graft_entry__.build()
+    yield
+    assert nvq.device_status() == 0
+
+
+def _sample_positions(R, C, n, seed):
+    rng = np.random.default_rng(seed)
+    r = rng.integers(0, R, n)
+    c = rng.integers(0, C, n)
+    row = int(rng.integers(0, R))
+    col = int(rng.integers(0, C))
+    rows = np.concatenate([r, np.full(C, row), np.arange(R)])
+    cols = np.concatenate([c, np.arange(C), np.full(R, col)])
+    return rows, cols
+
+
+def _check_sampled(got: torch.Tensor, fmt, a, b, K, rows, cols, what):
+    """a, b: oracle (codes, compact scales, amax) operands; got: bf16 GPU output."""
+    ga = oracle.nvfp4_g(a[2]) if fmt == 1 else 1.0
+    gb = oracle.nvfp4_g(b[2]) if fmt == 1 else 1.0
+    ref = oracle.gemm_tn_sampled(fmt, a[0], a[1], ga, b[0], b[1], gb, K, rows, cols)
+    g = got[torch.from_numpy(rows), torch.from_numpy(cols)].float().cpu().numpy().astype(np.float64)
+    refb = bf16_from_bits(oracle.to_bf16_rne(ref)).float().numpy().astype(np.float64)
+    rel = np.linalg.norm(g - refb) / np.linalg.norm(refb)
+    assert rel <= 1e-3, f"{what}: sampled relative Frobenius error {rel:.3e}"
+    gb_ = bits(got[torch.from_numpy(rows), torch.from_numpy(cols)]).astype(np.int32)
+    rb = oracle.to_bf16_rne(ref).astype(np.int32)
+
+    def ordered(v):
+        return np.where(v & 0x8000, -(v & 0x7FFF), v & 0x7FFF)
+
+    frac = np.mean(np.abs(ordered(gb_) - ordered(rb)) <= 1)
+    assert frac >= 0.999, f"{what}: {frac:.5f} of sampled outputs within 1 bf16 ulp"
+
+
+def test_llama3_8b_up_step_full_size():
+    M, N, K = inputs.LLAMA3_8B_UP["M"], inputs.LLAMA3_8B_UP["N"], inputs.LLAMA3_8B_UP["K"]
+    x, w, dy = inputs.llama_up()
+    sign = inputs.rht_sign_vector()
+    sr = (inputs.SR_SEED, 0)
+    y, saved = nvq.nvfp4_linear_fwd(x.cuda(), w.cuda(), rht_sign=sign)
+    bw = nvq.nvfp4_linear_bwd_quantize(dy.cuda(), rht_sign=sign, sr=sr)
+    dx = nvq.nvfp4_linear_dgrad(bw["dy_row"], saved["w_col"])
+    dw = nvq.nvfp4_linear_wgrad(bw["dy_col"], saved["x_col"])
+    torch.cuda.synchronize()
+
+    xb, wb, dyb = bits(x), bits(w), bits(dy)
+    ops = {
+        "x_row": (saved["x_row"], oracle.nvfp4_quantize_rows(xb)),
+        "x_col": (saved["x_col"], oracle.nvfp4_quantize_cols(xb, rht_sign=sign)),
+        "w_row": (saved["w_row"], oracle.nvfp4_quantize_rows(wb)),
+        "w_col": (saved["w_col"], oracle.nvfp4_quantize_cols(wb)),
+        "dy_row": (bw["dy_row"], oracle.nvfp4_quantize_rows(dyb, sr=sr)),
+        "dy_col": (bw["dy_col"], oracle.nvfp4_quantize_cols(dyb, rht_sign=sign, sr=sr)),
+    }
+    for name, (q, (c, s, A)) in ops.items():
+        assert q.amax.item() == np.float32(A), name
+        assert_codes_equal(qt_codes(q), c, name + " codes")
+        assert_scales_equal(q, s, name + " scales")
+
+    _check_sampled(y.cpu(), 1, ops["x_row"][1], ops["w_row"][1], K, *_sample_positions(M, N, 4096, 1), "fwd y")
+    _check_sampled(dx.cpu(), 1, ops["dy_row"][1], ops["w_col"][1], N, *_sample_positions(M, K, 4096, 2), "dgrad dx")
+    _check_sampled(dw.cpu(), 1, ops["dy_col"][1], ops["x_col"][1], M, *_sample_positions(N, K, 4096, 3), "wgrad dW")
+
+
+def test_moe_grouped_full_size():
+    sizes, x, w, dy = inputs.moe_grouped()
+    G, Nn, K = w.shape
+    sizes = [int(v) for v in sizes]
+    xr, xc = nvq.grouped_hybrid_quantize(x.cuda(), sizes, nvq.NVFP4, nvq.MXFP8)
+    wr, wc = nvq.grouped_hybrid_quantize(w.reshape(G * Nn, K).cuda(), [Nn] * G, nvq.NVFP4, nvq.MXFP8)
+    dyr, dyc = nvq.grouped_hybrid_quantize(dy.cuda(), sizes, nvq.MXFP8, nvq.MXFP8)
+    y = nvq.grouped_gemm_rows(xr, wr, sizes, Nn, b_col_groups=False)
+    dx = nvq.grouped_gemm_rows(dyr, wc, sizes, Nn, b_col_groups=True)
+    dw = nvq.grouped_gemm_wgrad(dyc, xc, sizes)
+    torch.cuda.synchronize()
+    assert y.shape == (sum(sizes), Nn) and dx.shape == (sum(sizes), K) and dw.shape == (G, Nn, K)
+
+    order = np.argsort(sizes)
+    picks = sorted(set([int(order[0]), int(order[1]), int(order[-1]), int(order[len(order) // 2]), 5, 40]))
+    offs = np.concatenate([[0], np.cumsum(sizes)])
+    poffs = np.concatenate([[0], np.cumsum([-(-m // 128) * 128 for m in sizes])])
+    xb, wb, dyb = bits(x), bits(w), bits(dy)
+    xr_c, dyr_c = qt_codes(xr), qt_codes(dyr)
+    for g in picks:
+        m, s0, p0 = sizes[g], int(offs[g]), int(poffs[g])
+        if m == 0:
+            assert torch.count_nonzero(dw[g]).item() == 0
+            continue
+        # forward operands (NVFP4 rows) and output
+        a = oracle.nvfp4_quantize_rows(xb[s0:s0 + m])
+        b = oracle.nvfp4_quantize_rows(wb[g])
+        assert_codes_equal(xr_c[p0:p0 + m], a[0], f"expert {g} x_row codes")
+        assert xr.amax[g].item() == np.float32(a[2]) and wr.amax[g].item() == np.float32(b[2])
+        rows, cols = _sample_positions(m, Nn, 512, 10 + g)
+        _check_sampled(y[s0:s0 + m].cpu(), 1, a, b, K, rows, cols, f"expert {g} fwd")
+        # dgrad: MXFP8 dy rows x MXFP8 W columns
+        da = oracle.mxfp8_quantize_rows(dyb[s0:s0 + m]) + (0.0,)
+        db = oracle.mxfp8_quantize_cols(wb[g]) + (0.0,)
+        assert_codes_equal(dyr_c[p0:p0 + m], da[0], f"expert {g} dy_row codes")
+        rows, cols = _sample_positions(m, K, 512, 20 + g)
+        _check_sampled(dx[s0:s0 + m].cpu(), 2, da, db, Nn, rows, cols, f"expert {g} dgrad")
+        # wgrad: MXFP8 columns over the expert's 128-padded tokens
+        mp = -(-m // 128) * 128
+        xp = np.zeros((mp, K), np.uint16); xp[:m] = xb[s0:s0 + m]
+        dp = np.zeros((mp, Nn), np.uint16); dp[:m] = dyb[s0:s0 + m]
+        wa = oracle.mxfp8_quantize_cols(dp) + (0.0,)
+        wbb = oracle.mxfp8_quantize_cols(xp) + (0.0,)
+        rows, cols = _sample_positions(Nn, K, 512, 30 + g)
+        _check_sampled(dw[g].cpu(), 2, wa, wbb, mp, rows, cols, f"expert {g} wgrad")
