@@ -11,23 +11,26 @@
 // Structure: a persistent kernel, one CTA per SM, each CTA walking output
 // tiles of 128 x BN (BN = 256 when the output width allows, else 128) in a
 // static round-robin order (column tiles fastest, so the CTAs in flight share
-// A rows and sweep B from L2).  10 warps:
+// A rows and sweep B from L2).  14 warps:
 //   warp 0      TMA producer: A (128 rows x 128 bytes) and B (BN rows x 128
 //               bytes) tiles with cp.async.bulk.tensor (128B swizzle) and the
 //               matching 512-byte 128x4 block-scale tiles with cp.async.bulk
 //               into a ring of smem stages (full/empty mbarriers);
-//   warp 1      TMEM owner and MMA issuer: per stage copies the scale tiles
-//               smem -> TMEM (tcgen05.cp 32x128b.warpx4; each ring stage owns
-//               its TMEM columns so a refill never overwrites scales in use)
-//               and issues 4 block-scaled MMAs (NVFP4: kind::mxf4nvf4
-//               scale_vec::4X, K = 64; MXFP8: kind::mxf8f6f4 scale_vec::1X,
-//               K = 32, the scale byte chosen by the scale-factor id),
-//               accumulating fp32 into one of the TMEM accumulator stages;
-//   warps 2..9  epilogue: warp w reads TMEM lane quadrant w % 4, half
-//               (w - 2) / 4 of the columns; it loads its whole slice, releases
-//               the accumulator to the MMA warp, then scales by alpha, adds
-//               the bias and stores bf16 / fp32 rows while the next tile's
-//               MMAs run.
+//   warp 1      TMEM owner and MMA issuer: 4 block-scaled MMAs per stage
+//               (NVFP4: kind::mxf4nvf4 scale_vec::4X, K = 64; MXFP8:
+//               kind::mxf8f6f4 scale_vec::1X, K = 32, the scale byte chosen by
+//               the scale-factor id) into one of the TMEM accumulator stages;
+//   warps 2..5  scale staging: the MMA reads the scale of tile row r from
+//               TMEM lane r, column (scale base + r / 32); warp w owns lane
+//               quadrant w % 4 and, per stage, writes just that column of each
+//               128x4 scale tile with tcgen05.st (the smem->TMEM tcgen05.cp
+//               path replicates each tile four times and runs in the MMA's
+//               in-order pipe, where it cost more than the MMAs themselves);
+//   warps 6..13 epilogue: warp w reads TMEM lane quadrant w % 4, half
+//               (w - 6) / 4 of the columns, in 64-column passes; after its last
+//               load it releases the accumulator to the MMA warp, then scales
+//               by alpha, adds the bias and stores bf16 / fp32 rows while the
+//               next tile's MMAs run.
 // Every mbarrier wait is bounded; a wait that runs out records
 // NVQ_ERR_TIMEOUT and raises a CTA-wide abort flag so all roles leave their
 // loops; the producer then waits (bounded) for its copies in flight and the
@@ -43,8 +46,10 @@ namespace gemm {
 
 constexpr int BM = 128;
 constexpr int kTileBytesA = 128 * 128;
+constexpr int kScaleWarps = 4;
 constexpr int kEpiWarps = 8;
-constexpr int kThreads = 64 + 32 * kEpiWarps;
+constexpr int kFirstEpiWarp = 2 + kScaleWarps;
+constexpr int kThreads = 32 * (kFirstEpiWarp + kEpiWarps);
 constexpr uint32_t kTmemCols = 512;
 
 template <int FMT, int BN>
@@ -70,7 +75,7 @@ struct Cfg {
     static constexpr int kSfa = kB + kStages * kTileBytesB;
     static constexpr int kSfb = kSfa + kStages * kSfaBytes;
     static constexpr int kBar = kSfb + kStages * kSfbBytes;
-    static constexpr int kNumBars = 2 * kStages + 2 * kAccStages + 1;
+    static constexpr int kNumBars = 3 * kStages + 2 * kAccStages + 1;  // full, empty, sf_ready, acc x2, done
     static constexpr int kMisc = kBar + kNumBars * 8;  // tmem address, abort flag
     static constexpr int kAlloc = kMisc + 16 + 1024;
     static_assert(kAlloc <= 232448, "shared memory budget");
@@ -148,7 +153,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kBar);
     uint64_t* empty = full + C::kStages;
-    uint64_t* acc_full = empty + C::kStages;
+    uint64_t* sf_ready = empty + C::kStages;
+    uint64_t* acc_full = sf_ready + C::kStages;
     uint64_t* acc_empty = acc_full + C::kAccStages;
     uint64_t* mma_done = acc_empty + C::kAccStages;
     uint32_t* tmem_ptr = reinterpret_cast<uint32_t*>(smem + C::kMisc);
@@ -161,6 +167,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
+            mbar_init(&sf_ready[s], kScaleWarps);
         }
         for (int s = 0; s < C::kAccStages; ++s) {
             mbar_init(&acc_full[s], 1);
@@ -235,25 +242,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t d_tmem = tmem_base + (uint32_t)(as * BN);
                 for (int kb = 0; kb < tl.num_kb; ++kb, ++it) {
                     const int s = it % C::kStages;
-                    if (!wait_or_abort(&full[s], (it / C::kStages) & 1, args.status, abort_flag)) {
+                    const uint32_t par = (it / C::kStages) & 1;
+                    if (!wait_or_abort(&full[s], par, args.status, abort_flag) ||
+                        !wait_or_abort(&sf_ready[s], par, args.status, abort_flag)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     const int left = tl.k_len - kb * C::kStageK;
                     const int n_mma = min(C::kStageK, left) / C::kMmaK;
-                    const int atoms = (min(C::kStageK, left) + C::kElemPerAtom - 1) / C::kElemPerAtom;
                     const uint32_t sfa_col = tmem_base + C::kSfCol0 + (uint32_t)s * C::kSfColsPerStage;
                     const uint32_t sfb_col = sfa_col + C::kSfaCols;
-                    const uint32_t sfa_smem = smem_u32(smem + C::kSfa + s * C::kSfaBytes);
-                    const uint32_t sfb_smem = smem_u32(smem + C::kSfb + s * C::kSfbBytes);
-                    for (int j = 0; j < atoms; ++j) {
-                        tc_cp_32x128b_warpx4(sfa_col + 4 * j, smem_desc(sfa_smem + 512 * j, 16, 128, kSwizzleNone));
-#pragma unroll
-                        for (int h = 0; h < C::kBHalves; ++h)
-                            tc_cp_32x128b_warpx4(sfb_col + 4 * (C::kBHalves * j + h),
-                                                 smem_desc(sfb_smem + 512 * (h * C::kAtomsK + j), 16, 128, kSwizzleNone));
-                    }
                     const uint32_t a_smem = smem_u32(smem + C::kA + s * kTileBytesA);
                     const uint32_t b_smem = smem_u32(smem + C::kB + s * C::kTileBytesB);
                     for (int j = 0; j < n_mma; ++j) {
@@ -274,12 +273,56 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_commit(mma_done);
             mbar_wait(mma_done, 0, args.status);
         }
+    } else if (warp < kFirstEpiWarp) {
+        // ------------------------------------------------ scale staging (warps 2..5)
+        // A 512-byte 128x4 scale tile is 32 rows of 16 bytes; row l holds tile
+        // rows l, l+32, l+64, l+96 (one 32-bit word each: the scales of the
+        // tile's four k-steps).  The MMA of lane quadrant q reads word q of
+        // row l from TMEM lane 32 q + l; warp w writes the whole 16-byte row l
+        // into lane l of its quadrant w % 4 (4 columns, tcgen05.st), which is
+        // the layout a replicating smem->TMEM copy produces, without the MMA
+        // pipe.
+        const int q = warp & 3;
+        uint32_t it = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+            const Tile tl = decode<BN, C::kStageK>(args, t);
+            for (int kb = 0; kb < tl.num_kb; ++kb, ++it) {
+                const int s = it % C::kStages;
+                int good = 1;
+                if (lane == 0) good = wait_or_abort(&full[s], (it / C::kStages) & 1, args.status, abort_flag);
+                good = __shfl_sync(0xFFFFFFFFu, good, 0);
+                if (!good) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const int left = tl.k_len - kb * C::kStageK;
+                const int atoms = (min(C::kStageK, left) + C::kElemPerAtom - 1) / C::kElemPerAtom;
+                const uint32_t sfa_col = tmem_base + C::kSfCol0 + (uint32_t)s * C::kSfColsPerStage;
+                const uint32_t sfb_col = sfa_col + C::kSfaCols;
+                const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+                const uint8_t* sfa = smem + C::kSfa + s * C::kSfaBytes + lane * 16;
+                const uint8_t* sfb = smem + C::kSfb + s * C::kSfbBytes + lane * 16;
+                for (int j = 0; j < atoms; ++j) {
+                    tmem_st_32x32b_x4(sfa_col + lane_base + 4 * j, *reinterpret_cast<const uint4*>(sfa + 512 * j));
+#pragma unroll
+                    for (int h = 0; h < C::kBHalves; ++h)
+                        tmem_st_32x32b_x4(sfb_col + lane_base + 4 * (C::kBHalves * j + h),
+                                          *reinterpret_cast<const uint4*>(sfb + 512 * (h * C::kAtomsK + j)));
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sf_ready[s]);
+            }
+        }
     } else {
-        // ------------------------------------------------ epilogue (warps 2..9)
+        // ------------------------------------------------ epilogue (warps 6..13)
         constexpr int kCols = BN / 2;       // columns per warp
-        constexpr int kChunks = kCols / 32;
+        constexpr int kPasses = kCols / 64;  // 64-column passes
         const int quad = warp & 3;
-        const int half = (warp - 2) >> 2;
+        const int half = (warp - kFirstEpiWarp) >> 2;
         const int r = quad * 32 + lane;     // tile row = TMEM lane
         uint32_t tl_i = 0;
         for (int t = blockIdx.x; t < total; t += gridDim.x, ++tl_i) {
@@ -292,25 +335,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
             if (!ok) break;
             tc_fence_after();
-            uint32_t v[kCols];
-            if (tl.num_kb > 0) {
-                const uint32_t taddr = tmem_base + (uint32_t)(as * BN + half * kCols) + ((uint32_t)(quad * 32) << 16);
-#pragma unroll
-                for (int c = 0; c < kChunks; ++c) {
-                    uint32_t (&vc)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[c * 32]);
-                    tmem_ld_32x32b_x32(taddr + (uint32_t)(c * 32), vc);
-                }
-                tmem_ld_wait();
-            } else {
-#pragma unroll
-                for (int i = 0; i < kCols; ++i) v[i] = 0u;  // empty contraction: zero
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&acc_empty[as]);
-
             const int out_row = tl.mt_local * BM + r;
-            if (out_row >= gr.rows_valid) continue;
+            const bool row_ok = out_row < gr.rows_valid;
             float alpha = 1.0f;
             if (FMT == 1) {
                 const float ga = __fdiv_rn(args.a_amax[gr.amax_idx], 2688.0f);
@@ -319,29 +345,49 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const int col0 = tl.n_tile * BN + half * kCols;
             const int64_t rowoff = gr.c_off + (int64_t)out_row * args.ldc + col0;
-#pragma unroll
-            for (int c = 0; c < kChunks; ++c) {
-                float f[32];
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    float y = __fmul_rn(alpha, __uint_as_float(v[c * 32 + i]));
-                    if (args.bias) y = __fadd_rn(y, __uint_as_float((uint32_t)args.bias[col0 + c * 32 + i] << 16));
-                    f[i] = y;
-                }
-                if (args.c_fp32) {
-                    float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(args.C) + rowoff + c * 32);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) dst[i] = make_float4(f[4 * i], f[4 * i + 1], f[4 * i + 2], f[4 * i + 3]);
+            const uint32_t taddr = tmem_base + (uint32_t)(as * BN + half * kCols) + ((uint32_t)(quad * 32) << 16);
+#pragma unroll 1
+            for (int p = 0; p < kPasses; ++p) {
+                uint32_t v[64];
+                if (tl.num_kb > 0) {
+                    tmem_ld_32x32b_x32(taddr + (uint32_t)(p * 64), *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+                    tmem_ld_32x32b_x32(taddr + (uint32_t)(p * 64 + 32), *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+                    tmem_ld_wait();
                 } else {
-                    uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(args.C) + rowoff + c * 32);
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        __nv_bfloat162 p0 = __floats2bfloat162_rn(f[8 * i + 0], f[8 * i + 1]);
-                        __nv_bfloat162 p1 = __floats2bfloat162_rn(f[8 * i + 2], f[8 * i + 3]);
-                        __nv_bfloat162 p2 = __floats2bfloat162_rn(f[8 * i + 4], f[8 * i + 5]);
-                        __nv_bfloat162 p3 = __floats2bfloat162_rn(f[8 * i + 6], f[8 * i + 7]);
-                        dst[i] = make_uint4(*reinterpret_cast<uint32_t*>(&p0), *reinterpret_cast<uint32_t*>(&p1),
-                                            *reinterpret_cast<uint32_t*>(&p2), *reinterpret_cast<uint32_t*>(&p3));
+                    for (int i = 0; i < 64; ++i) v[i] = 0u;  // empty contraction: zero
+                }
+                if (p == kPasses - 1) {  // accumulator fully read: hand it back to the MMA warp
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&acc_empty[as]);
+                }
+                if (!row_ok) continue;
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    const int cc = p * 64 + c * 32;  // column offset within this warp's slice
+                    float f[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        float y = __fmul_rn(alpha, __uint_as_float(v[c * 32 + i]));
+                        if (args.bias) y = __fadd_rn(y, __uint_as_float((uint32_t)args.bias[col0 + cc + i] << 16));
+                        f[i] = y;
+                    }
+                    if (args.c_fp32) {
+                        float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(args.C) + rowoff + cc);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) dst[i] = make_float4(f[4 * i], f[4 * i + 1], f[4 * i + 2], f[4 * i + 3]);
+                    } else {
+                        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(args.C) + rowoff + cc);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            __nv_bfloat162 p0 = __floats2bfloat162_rn(f[8 * i + 0], f[8 * i + 1]);
+                            __nv_bfloat162 p1 = __floats2bfloat162_rn(f[8 * i + 2], f[8 * i + 3]);
+                            __nv_bfloat162 p2 = __floats2bfloat162_rn(f[8 * i + 4], f[8 * i + 5]);
+                            __nv_bfloat162 p3 = __floats2bfloat162_rn(f[8 * i + 6], f[8 * i + 7]);
+                            dst[i] = make_uint4(*reinterpret_cast<uint32_t*>(&p0), *reinterpret_cast<uint32_t*>(&p1),
+                                                *reinterpret_cast<uint32_t*>(&p2), *reinterpret_cast<uint32_t*>(&p3));
+                        }
                     }
                 }
             }
