@@ -282,23 +282,25 @@ __device__ __forceinline__ uint32_t e2m1x8_rn(const float (&v)[8])
 }
 
 // Stochastic rounding of v onto the E2M1 grid with 16 random bits r: the
-// magnitude between neighbours lo <= |v| < hi rounds up iff r < 2^16 * frac
-// (equivalently r < ceil(2^16 frac) for integer r); saturates at 6; keeps the
-// sign.  Returns the grid value (exactly representable), to be encoded by RN.
-__device__ __forceinline__ float e2m1_sr_value(float v, uint32_t r)
+// magnitude between neighbours lo <= |v| < hi (spacing q) rounds up iff
+// r < ceil(2^16 (|v| - lo) / q); saturates at 6; keeps the sign.  Computed as
+// idx = ceil(|v|/q - r/2^16), magnitude idx * q, which is the same decision:
+// with |v|/q = n + f, ceil(n + f - r/2^16) = n + [f > r/2^16] and, r being an
+// integer, f > r/2^16 <=> r < ceil(2^16 f).  Every step is exact in fp32:
+// |v|/q is a power-of-two scaling, r/2^16 is built from the bit pattern
+// 1.r (no conversion instruction), |v|/q - r/2^16 needs at most 24
+// significant bits, and ceil() of a value in (-1, 16) is a round-up add of
+// 1.5 * 2^23.  q = max(2^(floor(log2 |v|) - 1), 1/2) comes from the exponent
+// bits.  Returns the grid value, to be encoded by round-to-nearest.
+__device__ __forceinline__ float e2m1_sr_value(float v, uint32_t r16)
 {
-    const float a = fabsf(v);
-    float mag;
-    if (a >= 6.0f) {
-        mag = 6.0f;
-    } else {
-        const float q = a < 2.0f ? 0.5f : (a < 4.0f ? 1.0f : 2.0f);
-        const float inv_q = a < 2.0f ? 2.0f : (a < 4.0f ? 1.0f : 0.5f);
-        const float lo = __fmul_rn(floorf(__fmul_rn(a, inv_q)), q);
-        const float frac16 = __fmul_rn(__fsub_rn(a, lo), __fmul_rn(inv_q, 65536.0f));
-        mag = ((float)r < frac16) ? __fadd_rn(lo, q) : lo;
-    }
-    return copysignf(mag, v);
+    const float a = fminf(fabsf(v), 6.0f);
+    const float q = fmaxf(__uint_as_float((__float_as_uint(a) & 0x7F800000u) - 0x00800000u), 0.5f);
+    const float inv_q = __uint_as_float(0x7F000000u - __float_as_uint(q));
+    const float rf = __fsub_rn(__uint_as_float(0x3F800000u | (r16 << 7)), 1.0f);
+    const float d = __fmaf_rn(a, inv_q, -rf);
+    const float c = __fsub_rn(__fadd_ru(d, 12582912.0f), 12582912.0f);
+    return copysignf(__fmul_rn(c, q), v);
 }
 
 // ------------------------------------------------------------------ Philox4x32-10
