@@ -393,6 +393,268 @@ def measure_e2e(args, nvq, x_h, w_h, dy_h, sign, sr, dev, stream, world):
             "api": "nvq_nvfp4_linear_fwd / _bwd_quantize / _dgrad / _wgrad with pinned host buffers"}
 
 
+# ---------------------------------------------------------------- other workloads
+def _graph_ms(fn, steps, warmup, eager=False):
+    """Warm up, capture fn into a CUDA graph and replay it `steps` times between
+    CUDA events on the current stream; ms per replay."""
+    import torch
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    g = None
+    if not eager:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        torch.cuda.synchronize()
+        for _ in range(warmup):
+            g.replay()
+    torch.cuda.synchronize()
+    s = torch.cuda.current_stream()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(s)
+    for _ in range(steps):
+        g.replay() if g is not None else fn()
+    t1.record(s)
+    torch.cuda.synchronize()
+    return t0.elapsed_time(t1) / steps
+
+
+def _flushed_ms(fn, reps, warmup):
+    """Per-call time with L2 flushed (a 512 MB write) before every timed call:
+    for inputs that fit in L2.  The call itself is replayed from a CUDA graph."""
+    import torch
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    torch.cuda.synchronize()
+    s = torch.cuda.current_stream()
+    tot = 0.0
+    for _ in range(reps):
+        flush.fill_(1)
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(s)
+        g.replay()
+        t1.record(s)
+        torch.cuda.synchronize()
+        tot += t0.elapsed_time(t1)
+    return tot / reps
+
+
+def run_quant_sweep(args, nvq, inputs):
+    """Standalone quantize sweep: [M,4096] 0.1*t(3) with outlier channels,
+    M in {2048, 8192, 32768, 131072}; NVFP4 row+col (RTN), NVFP4 row+col with
+    RHT (col) and SR, MXFP8 row+col.  Algorithmic bytes: NVFP4 2 reads + 2 x
+    (0.5 + 1/16) B written per element = 5.125 B; MXFP8 2 + 2 x (1 + 1/32) =
+    4.0625 B.  Inputs below 129 MB are timed with L2 flushed before each call."""
+    import torch
+    sign = inputs.rht_sign_vector()
+    sr = (inputs.SR_SEED, 0)
+    entries, tot_b, tot_ms = [], 0.0, 0.0
+    for Mq in inputs.QUANT_SWEEP_M:
+        x = inputs.student_t3_outliers(Mq).cuda()
+        Kq = x.shape[1]
+        nr = nvq.alloc_qtensor(nvq.NVFP4, Mq, Kq)
+        nc = nvq.alloc_qtensor(nvq.NVFP4, Kq, nvq.colwise_cols(nvq.NVFP4, Mq))
+        mr = nvq.alloc_qtensor(nvq.MXFP8, Mq, Kq)
+        mc = nvq.alloc_qtensor(nvq.MXFP8, Kq, nvq.colwise_cols(nvq.MXFP8, Mq))
+        variants = [
+            ("nvfp4_rtn", 5.125, lambda: nvq.nvfp4_quantize(x, 3, out_row=nr, out_col=nc)),
+            ("nvfp4_rht_sr", 5.125, lambda: nvq.nvfp4_quantize(x, 3, rht_sign=sign, sr=sr, out_row=nr, out_col=nc)),
+            ("mxfp8", 4.0625, lambda: nvq.mxfp8_quantize(x, 3, out_row=mr, out_col=mc)),
+        ]
+        for name, bpe, fn in variants:
+            small = Mq * Kq * 2 < 129e6
+            ms = _flushed_ms(fn, max(5, args.steps), args.warmup) if small else _graph_ms(fn, args.steps, args.warmup)
+            b = Mq * Kq * bpe
+            entries.append({"M": Mq, "variant": name, "ms": ms, "GB/s": b / (ms * 1e-3) / 1e9,
+                            "l2": "flushed" if small else "inputs larger than L2"})
+            tot_b += b
+            tot_ms += ms
+        del x, nr, nc, mr, mc
+        torch.cuda.empty_cache()
+    value = tot_b / (tot_ms * 1e-3) / 1e9
+    return {"metric": "quantize sweep GB/s (algorithmic bytes, NVFP4 RTN / RHT+SR / MXFP8, row+col)",
+            "value": value, "unit": "GB/s", "ms_per_step": tot_ms, "dtype": "bf16 -> nvfp4 / mxfp8",
+            "config": {"workload": "quantize_sweep_Mx4096_student_t3", "M": list(inputs.QUANT_SWEEP_M), "K": 4096},
+            "sweep": entries, "roofline_bound": "hbm", "step_bytes": tot_b}
+
+
+def run_moe_grouped(args, nvq, inputs):
+    """64 experts 4096->1536, 65536 Zipf(1.1) tokens: grouped hybrid quantize of
+    x (NVFP4 row + MXFP8 col), W (NVFP4 row + MXFP8 col), dy (MXFP8 row + col);
+    grouped NVFP4 forward, MXFP8 dgrad and wgrad (3 x 2*65536*1536*4096 FLOP)."""
+    import torch
+    sizes, x, w, dy = inputs.moe_grouped()
+    sizes = [int(v) for v in sizes]
+    G, Nn, Kk = w.shape
+    x, dy = x.cuda(), dy.cuda()
+    w2 = w.reshape(G * Nn, Kk).cuda()
+    del w
+    P = nvq.grouped_padded_rows(sizes)
+    xr = nvq.alloc_qtensor(nvq.NVFP4, P, Kk, n_amax=G); xc = nvq.alloc_qtensor(nvq.MXFP8, Kk, P)
+    wr = nvq.alloc_qtensor(nvq.NVFP4, G * Nn, Kk, n_amax=G); wc = nvq.alloc_qtensor(nvq.MXFP8, Kk, G * Nn)
+    dr = nvq.alloc_qtensor(nvq.MXFP8, P, Nn); dc = nvq.alloc_qtensor(nvq.MXFP8, Nn, P)
+    T = sum(sizes)
+    y = torch.empty(T, Nn, dtype=torch.bfloat16, device="cuda")
+    dx = torch.empty(T, Kk, dtype=torch.bfloat16, device="cuda")
+    dwt = torch.empty(G, Nn, Kk, dtype=torch.bfloat16, device="cuda")
+
+    def step():
+        nvq.grouped_hybrid_quantize(x, sizes, nvq.NVFP4, nvq.MXFP8, out_row=xr, out_col=xc)
+        nvq.grouped_hybrid_quantize(w2, [Nn] * G, nvq.NVFP4, nvq.MXFP8, out_row=wr, out_col=wc)
+        nvq.grouped_gemm_rows(xr, wr, sizes, Nn, b_col_groups=False, out=y)
+        nvq.grouped_hybrid_quantize(dy, sizes, nvq.MXFP8, nvq.MXFP8, out_row=dr, out_col=dc)
+        nvq.grouped_gemm_rows(dr, wc, sizes, Nn, b_col_groups=True, out=dx)
+        nvq.grouped_gemm_wgrad(dc, xc, sizes, out=dwt)
+
+    ms = _graph_ms(step, args.steps, args.warmup, args.eager)
+    flop = 3 * 2.0 * T * Nn * Kk
+    return {"metric": "MoE grouped hybrid linear fwd+dgrad+wgrad TFLOP/s (64 experts 4096->1536)",
+            "value": flop / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms,
+            "dtype": "nvfp4 fwd / mxfp8 bwd",
+            "config": {"workload": "moe_grouped_64x4096x1536_zipf1.1", "tokens": T, "experts": G,
+                       "group_sizes_min_max": [min(sizes), max(sizes)], "padded_rows": P},
+            "gpu_launches_per_step": 9}
+
+
+def run_qwen3_stack(args, nvq, inputs):
+    """Qwen3-8B-shaped linear stack: 36 layers, 16384 tokens; layers 0-29 NVFP4
+    (RHT on wgrad operands, SR on dy), layers 30-35 and the 151936x4096 lm_head
+    in bf16 (torch.matmul).  Attention core, norms and activations are not on
+    the path: the o input is the q output, the down input the up output.
+    FLOPs per step = 6 x tokens x parameters."""
+    import torch
+    cfg = inputs.QWEN3_8B_STACK
+    Tk, H = cfg["tokens"], cfg["hidden"]
+    n_nv = cfg["n_layers"] - cfg["bf16_tail"]
+    sign = inputs.rht_sign_vector()
+    sr = (inputs.SR_SEED, 0)
+    cc = nvq.colwise_cols
+    al = nvq.alloc_qtensor
+    h = inputs.normal_bf16_on((Tk, H), 1.0, 1, "cuda")
+    layers = []
+    params = 0
+    for l in range(cfg["n_layers"]):
+        ws = dict(inputs.qwen3_layer_weights(l, device="cuda"))
+        params += sum(t.numel() for t in ws.values())
+        layers.append(ws)
+    lm_head = inputs.normal_bf16_on((cfg["vocab"], H), 0.02, 3, "cuda")
+    params += lm_head.numel()
+    dys = {n: inputs.normal_bf16_on((Tk, n), 0.01, 2, "cuda") for n in {H, cfg["kv_dim"], cfg["mlp"]}}
+    dlog = inputs.normal_bf16_on((Tk, cfg["vocab"]), 0.01, 4, "cuda")
+
+    # per NVFP4 layer: quantized weights (row + col), saved activations (col), outputs
+    st = []
+    for l in range(n_nv):
+        ws = layers[l]
+        e = {"w": {}, "y": {}}
+        for n, W in ws.items():
+            No, Ki = W.shape
+            e["w"][n] = (al(nvq.NVFP4, No, Ki), al(nvq.NVFP4, Ki, cc(nvq.NVFP4, No)))
+            e["y"][n] = torch.empty(Tk, No, dtype=torch.bfloat16, device="cuda")
+        e["a"] = {k: (al(nvq.NVFP4, Tk, d), al(nvq.NVFP4, d, cc(nvq.NVFP4, Tk)))
+                  for k, d in (("h", H), ("attn", H), ("mlp", cfg["mlp"]))}
+        st.append(e)
+    bw = {d: dict(dy_row=al(nvq.NVFP4, Tk, d), dy_col=al(nvq.NVFP4, d, cc(nvq.NVFP4, Tk)))
+          for d in {H, cfg["kv_dim"], cfg["mlp"]}}
+    dxb = {d: torch.empty(Tk, d, dtype=torch.bfloat16, device="cuda") for d in (H, cfg["mlp"])}
+    dwb = {n: torch.empty_like(W) for n, W in layers[0].items()}
+    src = {"q": "h", "k": "h", "v": "h", "gate": "h", "up": "h", "o": "attn", "down": "mlp"}
+
+    def step():
+        # forward
+        for l in range(n_nv):
+            e, ws = st[l], layers[l]
+            nvq.nvfp4_quantize(h, 3, rht_sign=sign, out_row=e["a"]["h"][0], out_col=e["a"]["h"][1])
+            for n in ("q", "k", "v", "gate", "up", "o", "down"):
+                if n == "o":
+                    nvq.nvfp4_quantize(e["y"]["q"], 3, rht_sign=sign, out_row=e["a"]["attn"][0], out_col=e["a"]["attn"][1])
+                if n == "down":
+                    nvq.nvfp4_quantize(e["y"]["up"], 3, rht_sign=sign, out_row=e["a"]["mlp"][0], out_col=e["a"]["mlp"][1])
+                wr, wc = e["w"][n]
+                nvq.nvfp4_quantize(ws[n], 3, out_row=wr, out_col=wc)
+                nvq.gemm_tn(e["a"][src[n]][0], wr, out=e["y"][n])
+        tail = [torch.matmul(h if W.shape[1] == H else dys[cfg["mlp"]], W.t())
+                for l in range(n_nv, cfg["n_layers"]) for W in layers[l].values()]
+        logits = torch.matmul(h, lm_head.t())
+        # backward (reverse order)
+        torch.matmul(dlog, lm_head)
+        torch.matmul(dlog.t(), h)
+        for l in range(cfg["n_layers"] - 1, n_nv - 1, -1):
+            for n, W in layers[l].items():
+                d = dys[W.shape[0]]
+                xin = h if W.shape[1] == H else dys[cfg["mlp"]]
+                torch.matmul(d, W)
+                torch.matmul(d.t(), xin)
+        for l in range(n_nv - 1, -1, -1):
+            e = st[l]
+            for n in ("down", "o", "up", "gate", "v", "k", "q"):
+                No = layers[l][n].shape[0]
+                b = nvq.nvfp4_linear_bwd_quantize(dys[No], rht_sign=sign, sr=sr, bufs=bw[No])
+                wr, wc = e["w"][n]
+                nvq.nvfp4_linear_dgrad(b["dy_row"], wc, dx=dxb[layers[l][n].shape[1]])
+                nvq.nvfp4_linear_wgrad(b["dy_col"], e["a"][src[n]][1], dw=dwb[n])
+        del tail, logits
+
+    steps = max(2, min(args.steps, 5))
+    ms = _graph_ms(step, steps, min(args.warmup, 3), args.eager)
+    flop = 6.0 * Tk * params
+    return {"metric": "Qwen3-8B-shaped 36-layer linear stack fwd+bwd TFLOP/s (30 NVFP4 + 6 bf16 layers + bf16 lm_head)",
+            "value": flop / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms,
+            "dtype": "nvfp4 (layers 0-29) / bf16 (tail, lm_head)",
+            "config": {"workload": "qwen3_8b_linear_stack", "tokens": Tk, "layers": cfg["n_layers"],
+                       "nvfp4_layers": n_nv, "params": params}, "tokens_per_s": Tk / (ms * 1e-3)}
+
+
+def run_single_linear(args, nvq, inputs):
+    """x, W bf16[256,512]: quantize both rowwise and y = x W^T (latency)."""
+    x, w = inputs.single_linear()
+    x, w = x.cuda(), w.cuda()
+    xr = nvq.alloc_qtensor(nvq.NVFP4, 256, 512)
+    wr = nvq.alloc_qtensor(nvq.NVFP4, 256, 512)
+    import torch
+    y = torch.empty(256, 256, dtype=torch.bfloat16, device="cuda")
+
+    def step():
+        nvq.nvfp4_quantize(x, nvq.DIR_ROW, out_row=xr)
+        nvq.nvfp4_quantize(w, nvq.DIR_ROW, out_row=wr)
+        nvq.gemm_tn(xr, wr, out=y)
+
+    ms = _flushed_ms(step, max(20, args.steps), args.warmup)
+    return {"metric": "single NVFP4 linear forward latency (256x256x512)", "value": ms * 1e3, "unit": "us",
+            "higher_is_better": False, "ms_per_step": ms, "dtype": "nvfp4",
+            "config": {"workload": "single_linear_256x256x512"}}
+
+
+def run_workload(args, rank, world, local_rank):
+    import torch
+    import __graft_entry__
+    import mxfp8_block_scaled_bf16_gb300 as nvq
+    from mxfp8_block_scaled_bf16_gb300 import inputs
+    __graft_entry__.build()
+    torch.cuda.set_device(local_rank)
+    fn = {"quant_sweep": run_quant_sweep, "moe_grouped": run_moe_grouped, "qwen3_stack": run_qwen3_stack,
+          "single_linear": run_single_linear}[args.workload]
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    r = fn(args, nvq, inputs)
+    clk = clocks.stop()
+    if nvq.device_status() != 0:
+        raise RuntimeError("device status error")
+    if rank != 0:
+        return 0
+    line = {"metric": r.pop("metric"), "value": r.pop("value"), "unit": r.pop("unit"), "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "higher_is_better": r.pop("higher_is_better", True),
+            "scaling": "weak", "vs_baseline": None, "data": "synthetic", "clocks": clk, **r}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -402,6 +664,9 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end measurement")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip timing the CPU oracle")
     ap.add_argument("--eager", action="store_true", help="launch the step eagerly instead of replaying a CUDA graph")
+    ap.add_argument("--workload", default="llama_up",
+                    choices=["llama_up", "quant_sweep", "moe_grouped", "qwen3_stack", "single_linear"],
+                    help="llama_up (default: the headline line) or one of the other configurations")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3) if args.impl == "ours" else args.warmup
     world = _env_int("WORLD_SIZE", 1)
@@ -415,6 +680,8 @@ def main():
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl")
     try:
+        if args.workload != "llama_up":
+            return run_workload(args, rank, world, local_rank)
         return run_ours(args, rank, world, local_rank)
     finally:
         if world > 1:

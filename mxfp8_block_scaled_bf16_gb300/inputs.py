@@ -104,10 +104,32 @@ QWEN3_8B_STACK = dict(n_layers=36, hidden=4096, kv_dim=1024, mlp=12288, tokens=2
                       vocab=151936, bf16_tail=6)
 
 
-def qwen3_layer_weights(layer: int, hidden: int = 4096, kv_dim: int = 1024, mlp: int = 12288):
-    """The seven linears of one layer as (name, W[out,in]) ~ N(0, 0.02^2)."""
-    g = _gen(1000 + layer)
-    shapes = [("q", hidden, hidden), ("k", kv_dim, hidden), ("v", kv_dim, hidden),
-              ("o", hidden, hidden), ("gate", mlp, hidden), ("up", mlp, hidden),
-              ("down", hidden, mlp)]
-    return [(n, normal_bf16((o, i), 0.02, g)) for n, o, i in shapes]
+QWEN3_LINEARS = (("q", "hidden", "hidden"), ("k", "kv_dim", "hidden"), ("v", "kv_dim", "hidden"),
+                 ("o", "hidden", "hidden"), ("gate", "mlp", "hidden"), ("up", "mlp", "hidden"),
+                 ("down", "hidden", "mlp"))
+
+
+def qwen3_layer_weights(layer: int, hidden: int = 4096, kv_dim: int = 1024, mlp: int = 12288,
+                        device: str = "cpu"):
+    """The seven linears of one layer as (name, W[out,in]) ~ N(0, 0.02^2), drawn
+    from a generator seeded 1000 + layer on `device` (the full stack is 7.9e9
+    parameters, so the benchmark draws it on the GPU; the CPU and GPU streams
+    differ, both are seeded)."""
+    g = torch.Generator(device=device)
+    g.manual_seed(1000 + layer)
+    dims = {"hidden": hidden, "kv_dim": kv_dim, "mlp": mlp}
+    out = []
+    for n, o, i in QWEN3_LINEARS:
+        t = torch.randn(dims[o], dims[i], generator=g, dtype=torch.float32, device=device)
+        out.append((n, t.mul_(0.02).to(torch.bfloat16)))
+    return out
+
+
+def normal_bf16_on(shape, std: float, seed: int, device: str) -> torch.Tensor:
+    """N(0, std^2) bf16 drawn on `device` from a generator seeded `seed`."""
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    t = torch.randn(*shape, generator=g, dtype=torch.float32, device=device)
+    if std != 1.0:
+        t.mul_(std)
+    return t.to(torch.bfloat16)
