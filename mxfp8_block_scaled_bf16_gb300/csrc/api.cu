@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -27,6 +28,18 @@ struct DeviceInit {
     int num_sms = 0;
     cudaError_t err = cudaSuccess;
 };
+
+// The CTA-pair GEMM kernel is used only when NVQ_GEMM_PAIR=1 is set in the
+// environment: it is exact, but on the Llama-3-8B shapes its MMA stream runs
+// slower than the single-CTA kernel's.
+bool pair_gemm_enabled()
+{
+    static const bool on = [] {
+        const char* e = std::getenv("NVQ_GEMM_PAIR");
+        return e && e[0] == '1';
+    }();
+    return on;
+}
 DeviceInit g_dev[kMaxDevices];
 
 // Per-device one-time setup: the status word's address and the GEMM
@@ -42,6 +55,7 @@ cudaError_t device_setup(int** status, int* num_sms = nullptr)
         d.err = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.status), g_status_word);
         if (d.err == cudaSuccess) d.err = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev);
         if (d.err == cudaSuccess) d.err = init_gemm_attributes();
+        if (d.err == cudaSuccess) d.err = init_gemm_pair_attributes();
     });
     *status = d.status;
     if (num_sms) *num_sms = d.num_sms;
@@ -272,11 +286,14 @@ nvq_status gemm_prepare(const nvq_qtensor* A, const nvq_qtensor* B, int64_t n_ou
     g->b_amax = B->amax;
     if (n_out % 128) return NVQ_ERR_SHAPE;
     g->block_n = gemm_block_n(n_out);
+    g->use_pair = (g->block_n == 256 && pair_gemm_enabled()) ? 1 : 0;
     g->any_k = (A->rows > 0 && A->cols > 0 && B->rows > 0 && B->cols > 0) ? 1 : 0;
     const int64_t eb = f == NVQ_FMT_NVFP4 ? 2 : 1;  // elements per byte
+    // the pair kernel loads 128 rows of B per CTA; the single-CTA one block_n rows
+    const uint32_t b_box = g->use_pair ? 128u : (uint32_t)g->block_n;
     nvq_status s = NVQ_OK;
     if (g->any_k) s = make_operand_map(am, A->data, A->rows, A->cols / eb, 128);
-    if (s == NVQ_OK && g->any_k) s = make_operand_map(bm, B->data, B->rows, B->cols / eb, (uint32_t)g->block_n);
+    if (s == NVQ_OK && g->any_k) s = make_operand_map(bm, B->data, B->rows, B->cols / eb, b_box);
     return s;
 }
 
@@ -295,6 +312,14 @@ nvq_status gemm_launch(const CUtensorMap& am, const CUtensorMap& bm, GemmArgs& g
     int num_sms = 0;
     if (device_setup(&status, &num_sms) != cudaSuccess) return NVQ_ERR_CUDA;
     g.status = status;
+    // pair tiles: each group's 128-row tiles taken two at a time
+    int pm = 0;
+    for (int i = 0; i < g.G; ++i) {
+        g.groups[i].pm_tile0 = pm;
+        pm += (g.groups[i].m_tiles + 1) / 2;
+    }
+    g.total_pm_tiles = pm;
+    if (g.use_pair) return cuda_status(launch_gemm_pair(&am, &bm, g, num_sms, stream));
     return cuda_status(launch_gemm(&am, &bm, g, num_sms, stream));
 }
 

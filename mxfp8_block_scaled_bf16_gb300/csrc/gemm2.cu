@@ -1,0 +1,443 @@
+// gemm2.cu -- CTA-pair (tcgen05 cta_group::2) variant of the block-scaled
+// GEMM, for outputs whose width is a multiple of 256.
+//
+// Method: as gemm.cu ("Add an NVFP4 quantization converter", torchtitan PR
+// #3914; "Hybrid quantization", TransformerEngine PR #2817): TN-form
+// C = alpha * A B^T with NVFP4 or MXFP8 block-scaled operands.
+//
+// Two CTAs of a cluster form a pair that owns a 256 x 256 output tile: CTA c
+// stages rows [128c, 128c+128) of the A tile and rows [128c, 128c+128) of the
+// B tile; the leader (c = 0) issues 256x256 MMAs that read both CTAs' shared
+// memory and write each CTA's half of the accumulator into its own TMEM
+// (128 rows x 256 fp32 columns).  Per CTA a stage holds 32 KB of operands
+// (against 48 KB for a 128x256 tile in one CTA) plus the A scales of its rows
+// and the B scales of all 256 columns (the pair MMA reads the full B scale
+// set from each CTA's TMEM), so five stages fit (NVFP4) and each SM moves
+// less data from L2 per MMA FLOP.  On the Llama-3-8B shapes the pair MMA
+// stream itself ran slower than the single-CTA one, so this kernel is only
+// used when NVQ_GEMM_PAIR=1 is set; it is kept exact and tested.
+//
+// Signalling (every wait bounded, as in gemm.cu):
+//   full[s]      leader: A/B bytes of both CTAs (each CTA's TMA load signals the
+//                leader's barrier, .cta_group::2);
+//   sf_full[s]   per CTA: this CTA's block-scale tiles;
+//   sf_ready[s]  leader: the 4 scale warps of both CTAs wrote their TMEM scales;
+//   empty[s]     per CTA: the leader's MMAs of stage s finished (multicast commit);
+//   acc_full     per CTA: the tile's accumulator is complete (multicast commit);
+//   acc_empty    leader: the 8 epilogue warps of both CTAs read the accumulator.
+// A cluster barrier brackets the kernel so no CTA exits while its partner's
+// MMAs, copies or arrivals may still reach it.
+#include <cuda.h>
+
+#include "nvq_device.cuh"
+#include "nvq_kernels.h"
+
+namespace nvq {
+
+namespace gemm2 {
+
+constexpr int BM = 128;                  // rows per CTA (256 per pair)
+constexpr int BN = 256;                  // MMA N = output columns per pair tile
+constexpr int kHalfTileBytes = 128 * 128;
+constexpr int kScaleWarps = 4;
+constexpr int kEpiWarps = 8;
+constexpr int kFirstEpiWarp = 2 + kScaleWarps;
+constexpr int kThreads = 32 * (kFirstEpiWarp + kEpiWarps);
+constexpr uint32_t kTmemCols = 512;
+
+// SFB_FULL: each CTA's TMEM holds the B scales of all 256 columns (both
+// halves) -- the layout the pair MMA reads; holding only the scales of the B
+// half a CTA stages gives wrong products.
+#ifndef NVQ_PAIR_SFB_FULL
+#define NVQ_PAIR_SFB_FULL 1
+#endif
+
+template <int FMT, bool SFB_FULL>
+struct Cfg {
+    static constexpr int kStageK = FMT == 1 ? 256 : 128;
+    static constexpr int kMmaK = FMT == 1 ? 64 : 32;
+    static constexpr int kAtomsK = FMT == 1 ? 4 : 1;
+    static constexpr int kElemPerAtom = FMT == 1 ? 64 : 128;
+    static constexpr int kSfbHalves = SFB_FULL ? 2 : 1;
+    static constexpr int kSfaBytes = kAtomsK * 512;
+    static constexpr int kSfbBytes = kAtomsK * 512 * kSfbHalves;
+    static constexpr int kStageBytes = 2 * kHalfTileBytes + kSfaBytes + kSfbBytes;
+    static constexpr int kStagesFit = (232448 - 1024 - 512) / kStageBytes;
+    static constexpr int kStages = kStagesFit < 6 ? kStagesFit : 6;
+    static constexpr uint32_t kSfaCols = 4 * kAtomsK;
+    static constexpr uint32_t kSfbCols = 4 * kAtomsK * kSfbHalves;
+    static constexpr uint32_t kSfColsPerStage = kSfaCols + kSfbCols;
+    static constexpr uint32_t kSfCol0 = BN;
+    static_assert(kSfCol0 + kStages * kSfColsPerStage <= kTmemCols, "TMEM budget");
+    static constexpr int kA = 0;
+    static constexpr int kB = kA + kStages * kHalfTileBytes;
+    static constexpr int kSfa = kB + kStages * kHalfTileBytes;
+    static constexpr int kSfb = kSfa + kStages * kSfaBytes;
+    static constexpr int kBar = kSfb + kStages * kSfbBytes;
+    static constexpr int kNumBars = 4 * kStages + 3;  // full, empty, sf_full, sf_ready, acc_full, acc_empty, done
+    static constexpr int kMisc = kBar + kNumBars * 8;
+    static constexpr int kAlloc = kMisc + 16 + 1024;
+    static_assert(kAlloc <= 232448, "shared memory budget");
+};
+
+// Instruction descriptor: as gemm.cu with M = 256 (bits 24-28 = M >> 4).
+template <int FMT>
+__device__ __forceinline__ uint32_t make_idesc(uint32_t sf_id)
+{
+    uint32_t d = 0;
+    if (FMT == 1) d |= (1u << 7) | (1u << 10);
+    d |= (uint32_t)(BN >> 3) << 17;
+    if (FMT == 2) d |= 1u << 23;
+    d |= (uint32_t)(256 >> 4) << 24;
+    d |= (sf_id & 3) << 4;
+    d |= (sf_id & 3) << 29;
+    return d;
+}
+
+struct PairTile {
+    int g, mt_local, n_tile, a_row, b_row_pair, a_k0, b_k0, k_len, num_kb;
+};
+
+// Pair tile t: column tile fastest; rows of the pair = 128-row tiles
+// 2 * mp and 2 * mp + 1 of the group; CTA `rank` takes the second index.
+// A row tile past the group's end loads the group's last tile (in bounds)
+// and stores nothing.
+template <int STAGE_K>
+__device__ __forceinline__ PairTile decode(const GemmArgs& a, int t, uint32_t rank)
+{
+    PairTile r;
+    const int mp = t / a.n_tiles;
+    r.n_tile = t - mp * a.n_tiles;
+    int lo = 0, hi = a.G - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (a.groups[mid].pm_tile0 <= mp) lo = mid;
+        else hi = mid - 1;
+    }
+    const GemmGroup& gr = a.groups[lo];
+    r.g = lo;
+    r.mt_local = 2 * (mp - gr.pm_tile0) + (int)rank;
+    const int mt_load = r.mt_local < gr.m_tiles ? r.mt_local : gr.m_tiles - 1;
+    r.a_row = gr.a_row0 + mt_load * BM;
+    r.b_row_pair = gr.b_row0 + r.n_tile * BN;
+    r.a_k0 = gr.a_k0;
+    r.b_k0 = gr.b_k0;
+    r.k_len = gr.k_len;
+    r.num_kb = (gr.k_len + STAGE_K - 1) / STAGE_K;
+    return r;
+}
+
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, int* status, volatile int* abort_flag)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 0;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 63) == 63) {
+            if (*abort_flag) return false;
+            if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                record_error(status, kErrTimeout);
+                *abort_flag = 1;
+                return false;
+            }
+        }
+    }
+}
+
+// Arrive on barrier `bar` of the leader CTA (local arrive in the leader).
+__device__ __forceinline__ void arrive_leader(uint64_t* bar, uint32_t rank)
+{
+    if (rank == 0) mbar_arrive(bar);
+    else mbar_arrive_cluster(map_to_rank(bar, 0));
+}
+
+template <int FMT, bool SFB_FULL>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    gemm_pair_kernel(const __grid_constant__ CUtensorMap a_map, const __grid_constant__ CUtensorMap b_map,
+                     const __grid_constant__ GemmArgs args)
+{
+    using C = Cfg<FMT, SFB_FULL>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kBar);
+    uint64_t* empty = full + C::kStages;
+    uint64_t* sf_full = empty + C::kStages;
+    uint64_t* sf_ready = sf_full + C::kStages;
+    uint64_t* acc_full = sf_ready + C::kStages;
+    uint64_t* acc_empty = acc_full + 1;
+    uint64_t* mma_done = acc_empty + 1;
+    uint32_t* tmem_ptr = reinterpret_cast<uint32_t*>(smem + C::kMisc);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kMisc + 4);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const int pair = (int)cluster_id_x(), n_pairs = (int)num_clusters_x();
+    const int total = args.total_pm_tiles * args.n_tiles;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+            mbar_init(&sf_full[s], 1);
+            mbar_init(&sf_ready[s], 2 * kScaleWarps);
+        }
+        mbar_init(acc_full, 1);
+        mbar_init(acc_empty, 2 * kEpiWarps);
+        mbar_init(mma_done, 1);
+        *abort_flag = 0;
+        fence_mbarrier_init();
+        if (args.any_k) {
+            tma_prefetch_desc(&a_map);
+            tma_prefetch_desc(&b_map);
+        }
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(tmem_ptr, kTmemCols);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    cluster_sync();  // both CTAs' barriers initialised and TMEM allocated
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_ptr;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer (both CTAs)
+        if (lane == 0) {
+            uint32_t it = 0;
+            bool ok = true;
+            for (int t = pair; t < total && ok; t += n_pairs) {
+                const PairTile tl = decode<C::kStageK>(args, t, rank);
+                for (int kb = 0; kb < tl.num_kb; ++kb, ++it) {
+                    const int s = it % C::kStages;
+                    if (!wait_or_abort(&empty[s], ((it / C::kStages) & 1) ^ 1, args.status, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    const int ka = tl.a_k0 + kb * C::kStageK, kbb = tl.b_k0 + kb * C::kStageK;
+                    const int left = tl.k_len - kb * C::kStageK;
+                    const int atoms = min(C::kAtomsK, (left + C::kElemPerAtom - 1) / C::kElemPerAtom);
+                    const uint32_t sf_bytes = (uint32_t)atoms * 512u;
+                    if (rank == 0) mbar_arrive_expect_tx(&full[s], 4u * kHalfTileBytes);  // A + B of both CTAs
+                    mbar_arrive_expect_tx(&sf_full[s], sf_bytes * (1 + C::kSfbHalves));
+                    const uint32_t bar = map_to_rank(&full[s], 0);
+                    const int b_row = tl.b_row_pair + (int)rank * 128;
+                    tma_load_2d_pair(smem + C::kA + s * kHalfTileBytes, &a_map, bar, FMT == 1 ? ka / 2 : ka, tl.a_row);
+                    tma_load_2d_pair(smem + C::kB + s * kHalfTileBytes, &b_map, bar, FMT == 1 ? kbb / 2 : kbb, b_row);
+                    bulk_load(smem + C::kSfa + s * C::kSfaBytes,
+                              args.a_scale + ((int64_t)(tl.a_row / 128) * args.a_scale_ctiles + ka / C::kElemPerAtom) * 512,
+                              sf_bytes, &sf_full[s]);
+#pragma unroll
+                    for (int h = 0; h < C::kSfbHalves; ++h) {
+                        const int brow = SFB_FULL ? tl.b_row_pair + h * 128 : b_row;
+                        bulk_load(smem + C::kSfb + s * C::kSfbBytes + h * C::kAtomsK * 512,
+                                  args.b_scale + ((int64_t)(brow / 128) * args.b_scale_ctiles + kbb / C::kElemPerAtom) * 512,
+                                  sf_bytes, &sf_full[s]);
+                    }
+                }
+            }
+            // drain this CTA's scale copies; the leader also drains the A/B
+            // copies of both CTAs (they complete on its full barriers)
+            const uint32_t n = it < (uint32_t)C::kStages ? it : (uint32_t)C::kStages;
+            for (uint32_t i = 0; i < n; ++i) {
+                const uint32_t k = it - 1 - i;
+                mbar_wait(&sf_full[k % C::kStages], (k / C::kStages) & 1, args.status);
+                if (rank == 0) mbar_wait(&full[k % C::kStages], (k / C::kStages) & 1, args.status);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer (leader CTA)
+        if (lane == 0 && rank == 0) {
+            uint32_t it = 0, tl_i = 0;
+            bool ok = true;
+            for (int t = pair; t < total && ok; t += n_pairs, ++tl_i) {
+                const PairTile tl = decode<C::kStageK>(args, t, 0);
+                if (!wait_or_abort(acc_empty, (tl_i & 1) ^ 1, args.status, abort_flag)) break;
+                tc_fence_after();
+                for (int kb = 0; kb < tl.num_kb; ++kb, ++it) {
+                    const int s = it % C::kStages;
+                    const uint32_t par = (it / C::kStages) & 1;
+                    if (!wait_or_abort(&full[s], par, args.status, abort_flag) ||
+                        !wait_or_abort(&sf_ready[s], par, args.status, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const int left = tl.k_len - kb * C::kStageK;
+                    const int n_mma = min(C::kStageK, left) / C::kMmaK;
+                    const uint32_t sfa_col = tmem_base + C::kSfCol0 + (uint32_t)s * C::kSfColsPerStage;
+                    const uint32_t sfb_col = sfa_col + C::kSfaCols;
+                    const uint32_t a_smem = smem_u32(smem + C::kA + s * kHalfTileBytes);
+                    const uint32_t b_smem = smem_u32(smem + C::kB + s * kHalfTileBytes);
+                    for (int j = 0; j < n_mma; ++j) {
+                        const uint64_t ad = smem_desc(a_smem + 32 * j, 16, 1024, kSwizzle128B);
+                        const uint64_t bd = smem_desc(b_smem + 32 * j, 16, 1024, kSwizzle128B);
+                        const uint32_t acc = (kb > 0 || j > 0) ? 1u : 0u;
+                        if constexpr (FMT == 1)
+                            tc_mma_nvf4_pair(tmem_base, ad, bd, make_idesc<1>(0), sfa_col + 4 * j,
+                                             sfb_col + 4 * C::kSfbHalves * j, acc);
+                        else
+                            tc_mma_mxf8_pair(tmem_base, ad, bd, make_idesc<2>((uint32_t)j), sfa_col, sfb_col, acc);
+                    }
+                    tc_commit_pair(&empty[s], 0x3);
+                }
+                tc_commit_pair(acc_full, 0x3);
+            }
+            tc_commit_pair(mma_done, 0x1);
+            mbar_wait(mma_done, 0, args.status);
+        }
+    } else if (warp < kFirstEpiWarp) {
+        // ------------------------------------------------ scale staging (both CTAs)
+        const int q = warp & 3;
+        uint32_t it = 0;
+        bool ok = true;
+        for (int t = pair; t < total && ok; t += n_pairs) {
+            const PairTile tl = decode<C::kStageK>(args, t, rank);
+            for (int kb = 0; kb < tl.num_kb; ++kb, ++it) {
+                const int s = it % C::kStages;
+                int good = 1;
+                if (lane == 0) good = wait_or_abort(&sf_full[s], (it / C::kStages) & 1, args.status, abort_flag);
+                good = __shfl_sync(0xFFFFFFFFu, good, 0);
+                if (!good) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const int left = tl.k_len - kb * C::kStageK;
+                const int atoms = (min(C::kStageK, left) + C::kElemPerAtom - 1) / C::kElemPerAtom;
+                const uint32_t sfa_col = tmem_base + C::kSfCol0 + (uint32_t)s * C::kSfColsPerStage;
+                const uint32_t sfb_col = sfa_col + C::kSfaCols;
+                const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+                const uint8_t* sfa = smem + C::kSfa + s * C::kSfaBytes + lane * 16;
+                const uint8_t* sfb = smem + C::kSfb + s * C::kSfbBytes + lane * 16;
+                for (int j = 0; j < atoms; ++j) {
+                    tmem_st_32x32b_x4(sfa_col + lane_base + 4 * j, *reinterpret_cast<const uint4*>(sfa + 512 * j));
+#pragma unroll
+                    for (int h = 0; h < C::kSfbHalves; ++h)
+                        tmem_st_32x32b_x4(sfb_col + lane_base + 4 * (C::kSfbHalves * j + h),
+                                          *reinterpret_cast<const uint4*>(sfb + 512 * (h * C::kAtomsK + j)));
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) arrive_leader(&sf_ready[s], rank);
+            }
+        }
+    } else {
+        // ------------------------------------------------ epilogue (both CTAs)
+        constexpr int kCols = BN / 2;
+        constexpr int kPasses = kCols / 64;
+        const int quad = warp & 3;
+        const int half = (warp - kFirstEpiWarp) >> 2;
+        const int r = quad * 32 + lane;
+        uint32_t tl_i = 0;
+        for (int t = pair; t < total; t += n_pairs, ++tl_i) {
+            const PairTile tl = decode<C::kStageK>(args, t, rank);
+            const GemmGroup& gr = args.groups[tl.g];
+            int ok = 1;
+            if (lane == 0) ok = wait_or_abort(acc_full, tl_i & 1, args.status, abort_flag);
+            ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+            if (!ok) break;
+            tc_fence_after();
+            const int out_row = tl.mt_local * BM + r;
+            const bool row_ok = out_row < gr.rows_valid;
+            float alpha = 1.0f;
+            if (FMT == 1) {
+                const float ga = __fdiv_rn(args.a_amax[gr.amax_idx], 2688.0f);
+                const float gb = __fdiv_rn(args.b_amax[gr.amax_idx], 2688.0f);
+                alpha = __fmul_rn(ga, gb);
+            }
+            const int col0 = tl.n_tile * BN + half * kCols;
+            const int64_t rowoff = gr.c_off + (int64_t)out_row * args.ldc + col0;
+            const uint32_t taddr = tmem_base + (uint32_t)(half * kCols) + ((uint32_t)(quad * 32) << 16);
+#pragma unroll 1
+            for (int p = 0; p < kPasses; ++p) {
+                uint32_t v[64];
+                if (tl.num_kb > 0) {
+                    tmem_ld_32x32b_x32(taddr + (uint32_t)(p * 64), *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+                    tmem_ld_32x32b_x32(taddr + (uint32_t)(p * 64 + 32), *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+                    tmem_ld_wait();
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 64; ++i) v[i] = 0u;
+                }
+                if (p == kPasses - 1) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) arrive_leader(acc_empty, rank);
+                }
+                if (!row_ok) continue;
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    const int cc = p * 64 + c * 32;
+                    float f[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        float y = __fmul_rn(alpha, __uint_as_float(v[c * 32 + i]));
+                        if (args.bias) y = __fadd_rn(y, __uint_as_float((uint32_t)args.bias[col0 + cc + i] << 16));
+                        f[i] = y;
+                    }
+                    if (args.c_fp32) {
+                        float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(args.C) + rowoff + cc);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) dst[i] = make_float4(f[4 * i], f[4 * i + 1], f[4 * i + 2], f[4 * i + 3]);
+                    } else {
+                        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(args.C) + rowoff + cc);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            __nv_bfloat162 p0 = __floats2bfloat162_rn(f[8 * i + 0], f[8 * i + 1]);
+                            __nv_bfloat162 p1 = __floats2bfloat162_rn(f[8 * i + 2], f[8 * i + 3]);
+                            __nv_bfloat162 p2 = __floats2bfloat162_rn(f[8 * i + 4], f[8 * i + 5]);
+                            __nv_bfloat162 p3 = __floats2bfloat162_rn(f[8 * i + 6], f[8 * i + 7]);
+                            dst[i] = make_uint4(*reinterpret_cast<uint32_t*>(&p0), *reinterpret_cast<uint32_t*>(&p1),
+                                                *reinterpret_cast<uint32_t*>(&p2), *reinterpret_cast<uint32_t*>(&p3));
+                        }
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // the partner no longer issues MMAs, copies or arrivals that reach this CTA
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, kTmemCols);
+    }
+}
+
+template <int FMT>
+cudaError_t set_smem()
+{
+    using C = Cfg<FMT, NVQ_PAIR_SFB_FULL != 0>;
+    return cudaFuncSetAttribute(gemm_pair_kernel<FMT, NVQ_PAIR_SFB_FULL != 0>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, C::kAlloc);
+}
+
+}  // namespace gemm2
+
+cudaError_t init_gemm_pair_attributes()
+{
+    cudaError_t e = gemm2::set_smem<1>();
+    if (e == cudaSuccess) e = gemm2::set_smem<2>();
+    return e;
+}
+
+cudaError_t launch_gemm_pair(const void* a_map, const void* b_map, const GemmArgs& g, int num_sms, cudaStream_t s)
+{
+    const int tiles = g.total_pm_tiles * g.n_tiles;
+    if (tiles == 0) return cudaSuccess;
+    const int pairs = tiles < num_sms / 2 ? tiles : num_sms / 2;
+    const CUtensorMap& am = *reinterpret_cast<const CUtensorMap*>(a_map);
+    const CUtensorMap& bm = *reinterpret_cast<const CUtensorMap*>(b_map);
+    constexpr bool kFull = NVQ_PAIR_SFB_FULL != 0;
+    if (g.fmt == 1)
+        gemm2::gemm_pair_kernel<1, kFull>
+            <<<2 * pairs, gemm2::kThreads, gemm2::Cfg<1, kFull>::kAlloc, s>>>(am, bm, g);
+    else
+        gemm2::gemm_pair_kernel<2, kFull>
+            <<<2 * pairs, gemm2::kThreads, gemm2::Cfg<2, kFull>::kAlloc, s>>>(am, bm, g);
+    return cudaGetLastError();
+}
+
+}  // namespace nvq

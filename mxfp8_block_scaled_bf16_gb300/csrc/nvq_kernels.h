@@ -56,6 +56,7 @@ cudaError_t launch_quantize(const QuantArgs& a, int row_fmt, int col_fmt, bool r
 // One GEMM problem (or one group of a grouped GEMM) in TN form.
 struct GemmGroup {
     int32_t m_tile0;    // first 128-row output tile of this group (prefix over groups)
+    int32_t pm_tile0;   // first 256-row pair tile of this group (CTA-pair kernel)
     int32_t m_tiles;    // 128-row tiles of this group
     int32_t a_row0;     // first row of A (padded space)
     int32_t b_row0;     // first row of B
@@ -70,6 +71,8 @@ struct GemmGroup {
 struct GemmArgs {
     int fmt;               // 1 NVFP4, 2 MXFP8
     int block_n;           // output tile width BN (128 or 256)
+    int use_pair;          // run the CTA-pair kernel (block_n == 256)
+    int total_pm_tiles;    // sum over groups of ceil(m_tiles / 2)
     int any_k;             // some group has a nonzero contraction (tensor maps valid)
     int n_tiles;           // output column tiles (N / BN)
     int total_m_tiles;     // sum of m_tiles
@@ -96,5 +99,9 @@ int gemm_block_n(int64_t n_out);
 cudaError_t launch_gemm(const void* a_map, const void* b_map, const GemmArgs& g, int num_sms, cudaStream_t s);
 
 cudaError_t init_gemm_attributes();
+
+// CTA-pair (cta_group::2) kernel for block_n == 256: 2 * min(tiles, num_sms / 2) CTAs.
+cudaError_t launch_gemm_pair(const void* a_map, const void* b_map, const GemmArgs& g, int num_sms, cudaStream_t s);
+cudaError_t init_gemm_pair_attributes();
 
 }  // namespace nvq
