@@ -261,6 +261,16 @@ nvq_status quantize_impl(const void* x, int64_t M, int64_t K, int64_t ld, const 
     return cuda_status(launch_quantize(a, (int)row_fmt, (int)col_fmt, rht, sr != nullptr, row_tiles, stream));
 }
 
+// Test hook for the bounded waits: with NVQ_DEBUG_DROP_TMA=1 in the environment
+// (read at every GEMM call) the single-CTA GEMM kernel arms its first pipeline
+// stage but issues no copy into it, so every wait on that stage runs out, the
+// kernel records NVQ_ERR_TIMEOUT and returns.  Nothing faults or hangs.
+bool debug_drop_first_load()
+{
+    const char* e = std::getenv("NVQ_DEBUG_DROP_TMA");
+    return e && e[0] == '1';
+}
+
 nvq_status gemm_prepare(const nvq_qtensor* A, const nvq_qtensor* B, int64_t n_out, CUtensorMap* am, CUtensorMap* bm,
                         GemmArgs* g)
 {
@@ -286,7 +296,7 @@ nvq_status gemm_prepare(const nvq_qtensor* A, const nvq_qtensor* B, int64_t n_ou
     g->b_amax = B->amax;
     if (n_out % 128) return NVQ_ERR_SHAPE;
     g->block_n = gemm_block_n(n_out);
-    g->use_pair = (g->block_n == 256 && pair_gemm_enabled()) ? 1 : 0;
+    g->use_pair = (g->block_n == 256 && pair_gemm_enabled() && !debug_drop_first_load()) ? 1 : 0;
     g->any_k = (A->rows > 0 && A->cols > 0 && B->rows > 0 && B->cols > 0) ? 1 : 0;
     const int64_t eb = f == NVQ_FMT_NVFP4 ? 2 : 1;  // elements per byte
     // the pair kernel loads 128 rows of B per CTA; the single-CTA one block_n rows
@@ -312,6 +322,7 @@ nvq_status gemm_launch(const CUtensorMap& am, const CUtensorMap& bm, GemmArgs& g
     int num_sms = 0;
     if (device_setup(&status, &num_sms) != cudaSuccess) return NVQ_ERR_CUDA;
     g.status = status;
+    g.debug_drop_first_load = debug_drop_first_load() ? 1 : 0;
     // pair tiles: each group's 128-row tiles taken two at a time
     int pm = 0;
     for (int i = 0; i < g.G; ++i) {

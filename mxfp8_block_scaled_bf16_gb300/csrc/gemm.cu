@@ -209,6 +209,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t sf_bytes = (uint32_t)atoms * 512u;
                     mbar_arrive_expect_tx(&full[s], (uint32_t)(kTileBytesA + C::kTileBytesB) +
                                                         sf_bytes * (1 + C::kBHalves));
+                    if (args.debug_drop_first_load && it == 0) continue;  // the stage never completes
                     tma_load_2d(smem + C::kA + s * kTileBytesA, &a_map, &full[s], FMT == 1 ? ka / 2 : ka, tl.a_row);
                     tma_load_2d(smem + C::kB + s * C::kTileBytesB, &b_map, &full[s], FMT == 1 ? kbb / 2 : kbb, tl.b_row);
                     bulk_load(smem + C::kSfa + s * C::kSfaBytes,

@@ -88,6 +88,7 @@ struct GemmArgs {
     int64_t ldc;
     int c_fp32;
     int* status;           // device status word
+    int debug_drop_first_load;  // test hook: arm stage 0's barrier but issue no copy
     GemmGroup groups[kMaxGroups];
 };
 
