@@ -394,16 +394,18 @@ __device__ __forceinline__ uint32_t e2m1x8_rn(const float (&v)[8])
 // integer, f > r/2^16 <=> r < ceil(2^16 f).  Every step is exact in fp32:
 // |v|/q is a power-of-two scaling, r/2^16 is built from the bit pattern
 // 1.r (no conversion instruction), |v|/q - r/2^16 needs at most 24
-// significant bits, and ceil() of a value in (-1, 16) is a round-up add of
+// significant bits, and ceil() of a value in (-1, 4) is a round-up add of
 // 1.5 * 2^23.  q = max(2^(floor(log2 |v|) - 1), 1/2) comes from the exponent
-// bits.  Returns the grid value, to be encoded by round-to-nearest.
-__device__ __forceinline__ float e2m1_sr_value(float v, uint32_t r16)
+// bits.  |v| >= 6 is not clamped first: it lands on a grid multiple >= 6 (at
+// most 3 * 2^126, finite), which the saturating round-to-nearest encode maps
+// to 6 like the saturation rule.  r_mant holds r in mantissa bits 7..22
+// (r << 7).  Returns the grid value, to be encoded by round-to-nearest.
+__device__ __forceinline__ float e2m1_sr_value(float v, uint32_t r_mant)
 {
-    const float a = fminf(fabsf(v), 6.0f);
-    const float q = fmaxf(__uint_as_float((__float_as_uint(a) & 0x7F800000u) - 0x00800000u), 0.5f);
+    const float q = fmaxf(__uint_as_float((__float_as_uint(v) & 0x7F800000u) - 0x00800000u), 0.5f);
     const float inv_q = __uint_as_float(0x7F000000u - __float_as_uint(q));
-    const float rf = __fsub_rn(__uint_as_float(0x3F800000u | (r16 << 7)), 1.0f);
-    const float d = __fmaf_rn(a, inv_q, -rf);
+    const float rf = __fsub_rn(__uint_as_float(0x3F800000u | r_mant), 1.0f);
+    const float d = __fmaf_rn(fabsf(v), inv_q, -rf);
     const float c = __fsub_rn(__fadd_ru(d, 12582912.0f), 12582912.0f);
     return copysignf(__fmul_rn(c, q), v);
 }
@@ -451,11 +453,12 @@ __device__ __forceinline__ Philox4 philox4x32_10_rk(uint32_t c0, uint32_t c1, ui
     return {c0, c1, c2, c3};
 }
 
-// 16-bit random field f (0..7) of a Philox block.
-__device__ __forceinline__ uint32_t philox_field(const Philox4& p, int f)
+// 16-bit random field f (0..7) of a Philox block (field 2i is the low half
+// of word i, 2i+1 the high half), placed in mantissa bits 7..22.
+__device__ __forceinline__ uint32_t philox_field_mant(const Philox4& p, int f)
 {
     const uint32_t w = (f >> 1) == 0 ? p.x : (f >> 1) == 1 ? p.y : (f >> 1) == 2 ? p.z : p.w;
-    return (f & 1) ? (w >> 16) : (w & 0xFFFFu);
+    return ((f & 1) ? (w >> 9) : (w << 7)) & 0x007FFF80u;
 }
 
 }  // namespace nvq

@@ -225,7 +225,7 @@ __device__ __forceinline__ uint32_t nvfp4_encode8(const float (&v)[8], float e, 
         const Philox4 p = philox4x32_10_rk((uint32_t)blk, (uint32_t)(blk >> 32), (uint32_t)dir, a.sr_offset,
                                            a.sr_round_key);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) s[j] = e2m1_sr_value(s[j], philox_field(p, j));
+        for (int j = 0; j < 8; ++j) s[j] = e2m1_sr_value(s[j], philox_field_mant(p, j));
     }
     return e2m1x8_rn(s);
 }
