@@ -357,48 +357,80 @@ def time_quantize(nvq, x, w, dy, sign, sr, fb, bb, stream, reps=5):
 
 
 def measure_e2e(args, nvq, x_h, w_h, dy_h, sign, sr, dev, stream, world):
-    """Same step through the public linear API with host inputs: pinned host ->
-    device copies of x, W, dy and device -> host copies of y, dx, dW inside the
-    timed region."""
+    """Same step through the public linear API with host buffers: every step
+    copies its inputs x, W, dy from pinned host memory to the device and reads
+    its results y, dx, dW back, all inside the timed region.  Steps are
+    pipelined over two device buffer sets and three streams (copy-in, compute,
+    copy-out), so step i+1's uploads and step i's downloads overlap compute."""
     import torch
     xh, wh, dyh = x_h.pin_memory(), w_h.pin_memory(), dy_h.pin_memory()
-    yh = torch.empty(M, N, dtype=torch.bfloat16).pin_memory()
-    dxh = torch.empty(M, K, dtype=torch.bfloat16).pin_memory()
-    dwh = torch.empty(N, K, dtype=torch.bfloat16).pin_memory()
-    xd, wd, dyd = torch.empty_like(xh, device=dev), torch.empty_like(wh, device=dev), torch.empty_like(dyh, device=dev)
-    y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
-    fb = bb = None
+    outs_h = [(torch.empty(M, N, dtype=torch.bfloat16).pin_memory(),
+               torch.empty(M, K, dtype=torch.bfloat16).pin_memory(),
+               torch.empty(N, K, dtype=torch.bfloat16).pin_memory()) for _ in range(2)]
+    sets = []
+    for _ in range(2):
+        sets.append(dict(x=torch.empty_like(xh, device=dev), w=torch.empty_like(wh, device=dev),
+                         dy=torch.empty_like(dyh, device=dev),
+                         y=torch.empty(M, N, dtype=torch.bfloat16, device=dev),
+                         dx=torch.empty(M, K, dtype=torch.bfloat16, device=dev),
+                         dw=torch.empty(N, K, dtype=torch.bfloat16, device=dev), fb=None, bb=None))
+    s_in, s_comp, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev = lambda: torch.cuda.Event()
+    in_ready = [ev(), ev()]
+    comp_done = [ev(), ev()]
+    out_done = [ev(), ev()]
+    used = [False, False]
 
-    def step():
-        nonlocal fb, bb
-        xd.copy_(xh, non_blocking=True)
-        wd.copy_(wh, non_blocking=True)
-        dyd.copy_(dyh, non_blocking=True)
-        _, fb = nvq.nvfp4_linear_fwd(xd, wd, rht_sign=sign, y=y, bufs=fb)
-        bb = nvq.nvfp4_linear_bwd_quantize(dyd, rht_sign=sign, sr=sr, bufs=bb)
-        dx = nvq.nvfp4_linear_dgrad(bb["dy_row"], fb["w_col"])
-        dw = nvq.nvfp4_linear_wgrad(bb["dy_col"], fb["x_col"])
-        yh.copy_(y, non_blocking=True)
-        dxh.copy_(dx, non_blocking=True)
-        dwh.copy_(dw, non_blocking=True)
+    def step(i):
+        b = i & 1
+        d = sets[b]
+        with torch.cuda.stream(s_in):
+            if used[b]:
+                s_in.wait_event(comp_done[b])  # the previous step on this set has read its inputs
+            d["x"].copy_(xh, non_blocking=True)
+            d["w"].copy_(wh, non_blocking=True)
+            d["dy"].copy_(dyh, non_blocking=True)
+            in_ready[b].record(s_in)
+        with torch.cuda.stream(s_comp):
+            s_comp.wait_event(in_ready[b])
+            if used[b]:
+                s_comp.wait_event(out_done[b])  # its results have been read back
+            _, d["fb"] = nvq.nvfp4_linear_fwd(d["x"], d["w"], rht_sign=sign, y=d["y"], bufs=d["fb"], stream=s_comp)
+            d["bb"] = nvq.nvfp4_linear_bwd_quantize(d["dy"], rht_sign=sign, sr=sr, bufs=d["bb"], stream=s_comp)
+            nvq.nvfp4_linear_dgrad(d["bb"]["dy_row"], d["fb"]["w_col"], dx=d["dx"], stream=s_comp)
+            nvq.nvfp4_linear_wgrad(d["bb"]["dy_col"], d["fb"]["x_col"], dw=d["dw"], stream=s_comp)
+            comp_done[b].record(s_comp)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(comp_done[b])
+            yh, dxh, dwh = outs_h[b]
+            yh.copy_(d["y"], non_blocking=True)
+            dxh.copy_(d["dx"], non_blocking=True)
+            dwh.copy_(d["dw"], non_blocking=True)
+            out_done[b].record(s_out)
+        used[b] = True
 
-    for _ in range(max(1, args.warmup)):
-        step()
+    for i in range(max(2, args.warmup)):
+        step(i)
     torch.cuda.synchronize()
+    steps = max(2, min(args.steps, 10))
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    steps = max(1, min(args.steps, 10))
-    for _ in range(steps):
-        step()
-    t1.record(stream)
+    t0.record(s_in)
+    s_comp.wait_event(t0)
+    s_out.wait_event(t0)
+    for i in range(steps):
+        step(i)
+    s_in.wait_stream(s_out)
+    s_in.wait_stream(s_comp)
+    t1.record(s_in)
     torch.cuda.synchronize()
     ms = t0.elapsed_time(t1) / steps
     bi = (M * K + N * K + M * N) * 2
     bo = (M * N + M * K + N * K) * 2
     return {"value": world * STEP_FLOP / (ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": ms,
             "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
-            "api": "nvq_nvfp4_linear_fwd / _bwd_quantize / _dgrad / _wgrad with pinned host buffers"}
+            "api": "nvq_nvfp4_linear_fwd / _bwd_quantize / _dgrad / _wgrad with pinned host buffers; "
+                   "copy-in, compute and copy-out streams over two buffer sets"}
 
 
 # ---------------------------------------------------------------- other workloads
