@@ -26,7 +26,7 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "--fmad=false", "-Xcompiler", "-fPIC",
               "-Xcompiler", "-fvisibility=hidden", "-I", INCLUDE]
 SOURCES = ["api.cu", "quantize.cu", "gemm.cu", "gemm2.cu"]
-HEADERS = ["nvq_device.cuh", "nvq_kernels.h"]
+HEADERS = ["nvq_device.cuh", "nvq_kernels.h", "gemm_epilogue.cuh"]
 
 
 def _nvcc() -> str:

@@ -330,6 +330,10 @@ nvq_status gemm_launch(const CUtensorMap& am, const CUtensorMap& bm, GemmArgs& g
         pm += (g.groups[i].m_tiles + 1) / 2;
     }
     g.total_pm_tiles = pm;
+    // 32-byte epilogue stores need every row start 32-byte aligned
+    bool st32 = !g.c_fp32 && (reinterpret_cast<uintptr_t>(g.C) & 31) == 0 && g.ldc % 16 == 0;
+    for (int i = 0; i < g.G && st32; ++i) st32 = g.groups[i].c_off % 16 == 0;
+    g.c_st32 = st32 ? 1 : 0;
     if (g.use_pair) return cuda_status(launch_gemm_pair(&am, &bm, g, num_sms, stream));
     return cuda_status(launch_gemm(&am, &bm, g, num_sms, stream));
 }

@@ -11,32 +11,34 @@
 // Structure: a persistent kernel, one CTA per SM, each CTA walking output
 // tiles of 128 x BN (BN = 256 when the output width allows, else 128) in a
 // static round-robin order (column tiles fastest, so the CTAs in flight share
-// A rows and sweep B from L2).  14 warps:
+// A rows and sweep B from L2).  15 warps:
 //   warp 0      TMA producer: A (128 rows x 128 bytes) and B (BN rows x 128
-//               bytes) tiles with cp.async.bulk.tensor (128B swizzle) and the
-//               matching 512-byte 128x4 block-scale tiles with cp.async.bulk
-//               into a ring of smem stages (full/empty mbarriers);
+//               bytes) tiles with cp.async.bulk.tensor (128B swizzle) into a
+//               ring of smem stages (full/empty mbarriers);
 //   warp 1      TMEM owner and MMA issuer: 4 block-scaled MMAs per stage
 //               (NVFP4: kind::mxf4nvf4 scale_vec::4X, K = 64; MXFP8:
 //               kind::mxf8f6f4 scale_vec::1X, K = 32, the scale byte chosen by
 //               the scale-factor id) into one of the TMEM accumulator stages;
-//   warps 2..5  scale staging: the MMA reads the scale of tile row r from
-//               TMEM lane r, column (scale base + r / 32); warp w owns lane
-//               quadrant w % 4 and, per stage, writes just that column of each
-//               128x4 scale tile with tcgen05.st (the smem->TMEM tcgen05.cp
-//               path replicates each tile four times and runs in the MMA's
-//               in-order pipe, where it cost more than the MMAs themselves);
+//   warps 2..5  scale staging: each 128x4 scale tile goes to TMEM in the
+//               replicated layout the block-scaled MMA reads (every lane
+//               quadrant holds the tile's 32 16-byte rows); warp w writes its
+//               quadrant w % 4 with tcgen05.st (the smem->TMEM tcgen05.cp path
+//               runs in the MMA's in-order pipe, where it cost more than the
+//               MMAs themselves);
 //   warps 6..13 epilogue: warp w reads TMEM lane quadrant w % 4, half
-//               (w - 6) / 4 of the columns, in 64-column passes; after its last
-//               load it releases the accumulator to the MMA warp, then scales
-//               by alpha, adds the bias and stores bf16 / fp32 rows while the
-//               next tile's MMAs run.
+//               (w - 6) / 4 of the columns; after its last load it releases the
+//               accumulator to the MMA warp, then stores the scaled (+ bias)
+//               bf16 / fp32 rows while the next tile's MMAs run;
+//   warp 14     block-scale loader: the stage's A and B scale tiles with
+//               cp.async.bulk (a separate thread from the A/B producer, since
+//               every copy costs its issuing thread ~100 cycles).
 // Every mbarrier wait is bounded; a wait that runs out records
 // NVQ_ERR_TIMEOUT and raises a CTA-wide abort flag so all roles leave their
 // loops; the producer then waits (bounded) for its copies in flight and the
 // MMA warp for its tensor-core work before TMEM is freed.
 #include <cuda.h>
 
+#include "gemm_epilogue.cuh"
 #include "nvq_device.cuh"
 #include "nvq_kernels.h"
 
@@ -49,7 +51,8 @@ constexpr int kTileBytesA = 128 * 128;
 constexpr int kScaleWarps = 4;
 constexpr int kEpiWarps = 8;
 constexpr int kFirstEpiWarp = 2 + kScaleWarps;
-constexpr int kThreads = 32 * (kFirstEpiWarp + kEpiWarps);
+constexpr int kScaleLoadWarp = kFirstEpiWarp + kEpiWarps;  // block-scale copies
+constexpr int kThreads = 32 * (kScaleLoadWarp + 1);
 constexpr uint32_t kTmemCols = 512;
 
 template <int FMT, int BN>
@@ -75,7 +78,7 @@ struct Cfg {
     static constexpr int kSfa = kB + kStages * kTileBytesB;
     static constexpr int kSfb = kSfa + kStages * kSfaBytes;
     static constexpr int kBar = kSfb + kStages * kSfbBytes;
-    static constexpr int kNumBars = 3 * kStages + 2 * kAccStages + 1;  // full, empty, sf_ready, acc x2, done
+    static constexpr int kNumBars = 4 * kStages + 2 * kAccStages + 1;  // full, empty, sf_ready, sf_full, acc x2, done
     static constexpr int kMisc = kBar + kNumBars * 8;  // tmem address, abort flag
     static constexpr int kAlloc = kMisc + 16 + 1024;
     static_assert(kAlloc <= 232448, "shared memory budget");
@@ -107,11 +110,13 @@ __device__ __forceinline__ Tile decode(const GemmArgs& a, int t)
     Tile r;
     const int m_tile = t / a.n_tiles;
     r.n_tile = t - m_tile * a.n_tiles;
-    int lo = 0, hi = a.G - 1;
-    while (lo < hi) {  // last group whose first tile <= m_tile (empty groups own no tile)
-        const int mid = (lo + hi + 1) >> 1;
-        if (a.groups[mid].m_tile0 <= m_tile) lo = mid;
-        else hi = mid - 1;
+    // last group whose first tile <= m_tile (empty groups own no tile):
+    // fixed-length branchless search over at most kMaxGroups groups
+    int lo = 0;
+#pragma unroll
+    for (int step = kMaxGroups / 2; step >= 1; step >>= 1) {
+        const int mid = lo + step;
+        lo = (mid < a.G && a.groups[mid].m_tile0 <= m_tile) ? mid : lo;
     }
     const GemmGroup& gr = a.groups[lo];
     r.g = lo;
@@ -157,6 +162,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* acc_full = sf_ready + C::kStages;
     uint64_t* acc_empty = acc_full + C::kAccStages;
     uint64_t* mma_done = acc_empty + C::kAccStages;
+    uint64_t* sf_full = mma_done + 1;
     uint32_t* tmem_ptr = reinterpret_cast<uint32_t*>(smem + C::kMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kMisc + 4);
 
@@ -168,6 +174,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
             mbar_init(&sf_ready[s], kScaleWarps);
+            mbar_init(&sf_full[s], 1);
         }
         for (int s = 0; s < C::kAccStages; ++s) {
             mbar_init(&acc_full[s], 1);
@@ -191,88 +198,86 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem_base = *tmem_ptr;
 
     if (warp == 0) {
-        // ------------------------------------------------ TMA producer
+        // ------------------------------------------------ TMA producer (A and B tiles)
+        // Straight-line issue: waits are PTX loops (mbar_wait_flag) and every
+        // copy is guarded by the CTA's live flag instead of a branch.  Each
+        // copy costs its issuing thread on the order of 100 cycles, so the
+        // block-scale copies have their own thread (the scale loader warp).
         if (lane == 0) {
-            uint32_t it = 0;
-            bool ok = true;
-            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+            uint32_t it = 0, n_armed = 0;
+            for (int t = blockIdx.x; t < total; t += gridDim.x) {
                 const Tile tl = decode<BN, C::kStageK>(args, t);
                 for (int kb = 0; kb < tl.num_kb; ++kb, ++it) {
                     const int s = it % C::kStages;
-                    if (!wait_or_abort(&empty[s], ((it / C::kStages) & 1) ^ 1, args.status, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
+                    mbar_wait_flag(&empty[s], ((it / C::kStages) & 1) ^ 1, abort_flag);
+                    uint32_t live = live_flag(abort_flag);
+                    // test hook: live = 2 arms the stage but loads nothing
+                    live = (args.debug_drop_first_load && it == 0) ? 2u * live : live;
                     const int ka = tl.a_k0 + kb * C::kStageK, kbb = tl.b_k0 + kb * C::kStageK;
-                    const int left = tl.k_len - kb * C::kStageK;
-                    const int atoms = min(C::kAtomsK, (left + C::kElemPerAtom - 1) / C::kElemPerAtom);
-                    const uint32_t sf_bytes = (uint32_t)atoms * 512u;
-                    mbar_arrive_expect_tx(&full[s], (uint32_t)(kTileBytesA + C::kTileBytesB) +
-                                                        sf_bytes * (1 + C::kBHalves));
-                    if (args.debug_drop_first_load && it == 0) continue;  // the stage never completes
-                    tma_load_2d(smem + C::kA + s * kTileBytesA, &a_map, &full[s], FMT == 1 ? ka / 2 : ka, tl.a_row);
-                    tma_load_2d(smem + C::kB + s * C::kTileBytesB, &b_map, &full[s], FMT == 1 ? kbb / 2 : kbb, tl.b_row);
-                    bulk_load(smem + C::kSfa + s * C::kSfaBytes,
-                              args.a_scale + ((int64_t)(tl.a_row / 128) * args.a_scale_ctiles + ka / C::kElemPerAtom) * 512,
-                              sf_bytes, &full[s]);
-#pragma unroll
-                    for (int h = 0; h < C::kBHalves; ++h)
-                        bulk_load(smem + C::kSfb + s * C::kSfbBytes + h * C::kAtomsK * 512,
-                                  args.b_scale +
-                                      ((int64_t)(tl.b_row / 128 + h) * args.b_scale_ctiles + kbb / C::kElemPerAtom) * 512,
-                                  sf_bytes, &full[s]);
+                    mbar_arrive_expect_tx_if(&full[s], (uint32_t)(kTileBytesA + C::kTileBytesB), live);
+                    n_armed += live != 0 ? 1u : 0u;
+                    live = live == 1 ? 1u : 0u;
+                    tma_load_2d_if(smem + C::kA + s * kTileBytesA, &a_map, &full[s], FMT == 1 ? ka / 2 : ka, tl.a_row, live);
+                    tma_load_2d_if(smem + C::kB + s * C::kTileBytesB, &b_map, &full[s], FMT == 1 ? kbb / 2 : kbb, tl.b_row,
+                                   live);
                 }
             }
-            // drain: the last copy issued into each stage has landed before exit
-            const uint32_t n = it < (uint32_t)C::kStages ? it : (uint32_t)C::kStages;
+            // drain: the armed stages are a prefix of the iterations (abort is
+            // sticky); the last copy issued into each stage has landed before exit
+            const uint32_t n = n_armed < (uint32_t)C::kStages ? n_armed : (uint32_t)C::kStages;
             for (uint32_t i = 0; i < n; ++i) {
-                const uint32_t k = it - 1 - i;
+                const uint32_t k = n_armed - 1 - i;
                 mbar_wait(&full[k % C::kStages], (k / C::kStages) & 1, args.status);
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
+        // Straight-line issue as in the producer: the per-stage MMAs are
+        // unrolled (the short last stage of a ragged K predicates the rest
+        // off), descriptors advance by adding to the start-address field
+        // (smem addresses < 256 KB keep it within its 14 bits).
         if (lane == 0) {
+            constexpr int kMmas = C::kStageK / C::kMmaK;
+            const uint64_t a_desc0 = smem_desc(smem_u32(smem + C::kA), 16, 1024, kSwizzle128B);
+            const uint64_t b_desc0 = smem_desc(smem_u32(smem + C::kB), 16, 1024, kSwizzle128B);
             uint32_t it = 0, tl_i = 0;
-            bool ok = true;
-            for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++tl_i) {
+            for (int t = blockIdx.x; t < total; t += gridDim.x, ++tl_i) {
                 const Tile tl = decode<BN, C::kStageK>(args, t);
                 const int as = tl_i % C::kAccStages;
-                if (!wait_or_abort(&acc_empty[as], ((tl_i / C::kAccStages) & 1) ^ 1, args.status, abort_flag)) break;
+                mbar_wait_flag(&acc_empty[as], ((tl_i / C::kAccStages) & 1) ^ 1, abort_flag);
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(as * BN);
                 for (int kb = 0; kb < tl.num_kb; ++kb, ++it) {
                     const int s = it % C::kStages;
                     const uint32_t par = (it / C::kStages) & 1;
-                    if (!wait_or_abort(&full[s], par, args.status, abort_flag) ||
-                        !wait_or_abort(&sf_ready[s], par, args.status, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
+                    mbar_wait_flag(&full[s], par, abort_flag);
+                    mbar_wait_flag(&sf_ready[s], par, abort_flag);
                     tc_fence_after();
-                    const int left = tl.k_len - kb * C::kStageK;
-                    const int n_mma = min(C::kStageK, left) / C::kMmaK;
+                    const uint32_t live = live_flag(abort_flag);
+                    const int n_mma = min(C::kStageK, tl.k_len - kb * C::kStageK) / C::kMmaK;
                     const uint32_t sfa_col = tmem_base + C::kSfCol0 + (uint32_t)s * C::kSfColsPerStage;
                     const uint32_t sfb_col = sfa_col + C::kSfaCols;
-                    const uint32_t a_smem = smem_u32(smem + C::kA + s * kTileBytesA);
-                    const uint32_t b_smem = smem_u32(smem + C::kB + s * C::kTileBytesB);
-                    for (int j = 0; j < n_mma; ++j) {
-                        const uint64_t ad = smem_desc(a_smem + 32 * j, 16, 1024, kSwizzle128B);
-                        const uint64_t bd = smem_desc(b_smem + 32 * j, 16, 1024, kSwizzle128B);
+                    const uint64_t ad = a_desc0 + (uint64_t)((s * kTileBytesA) >> 4);
+                    const uint64_t bd = b_desc0 + (uint64_t)((s * C::kTileBytesB) >> 4);
+#pragma unroll
+                    for (int j = 0; j < kMmas; ++j) {
+                        const uint32_t on = (j < n_mma) ? live : 0u;
                         const uint32_t acc = (kb > 0 || j > 0) ? 1u : 0u;
                         if constexpr (FMT == 1)
-                            tc_mma_nvf4(d_tmem, ad, bd, make_idesc<1, BN>(0), sfa_col + 4 * j,
-                                        sfb_col + 4 * C::kBHalves * j, acc);
+                            tc_mma_nvf4_if(d_tmem, ad + 2 * j, bd + 2 * j, make_idesc<1, BN>(0), sfa_col + 4 * j,
+                                           sfb_col + 4 * C::kBHalves * j, acc, on);
                         else
-                            tc_mma_mxf8(d_tmem, ad, bd, make_idesc<2, BN>((uint32_t)j), sfa_col, sfb_col, acc);
+                            tc_mma_mxf8_if(d_tmem, ad + 2 * j, bd + 2 * j, make_idesc<2, BN>((uint32_t)j), sfa_col,
+                                           sfb_col, acc, on);
                     }
-                    tc_commit(&empty[s]);
+                    tc_commit_if(&empty[s], live);
                 }
-                tc_commit(&acc_full[as]);
+                tc_commit_if(&acc_full[as], live_flag(abort_flag));
             }
             // all of this thread's tensor-core work has finished before TMEM is freed
             tc_commit(mma_done);
             mbar_wait(mma_done, 0, args.status);
+            if (*abort_flag) record_error(args.status, kErrTimeout);
         }
     } else if (warp < kFirstEpiWarp) {
         // ------------------------------------------------ scale staging (warps 2..5)
@@ -291,7 +296,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int kb = 0; kb < tl.num_kb; ++kb, ++it) {
                 const int s = it % C::kStages;
                 int good = 1;
-                if (lane == 0) good = wait_or_abort(&full[s], (it / C::kStages) & 1, args.status, abort_flag);
+                if (lane == 0) good = wait_or_abort(&sf_full[s], (it / C::kStages) & 1, args.status, abort_flag);
                 good = __shfl_sync(0xFFFFFFFFu, good, 0);
                 if (!good) {
                     ok = false;
@@ -305,12 +310,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t lane_base = (uint32_t)(q * 32) << 16;
                 const uint8_t* sfa = smem + C::kSfa + s * C::kSfaBytes + lane * 16;
                 const uint8_t* sfb = smem + C::kSfb + s * C::kSfbBytes + lane * 16;
-                for (int j = 0; j < atoms; ++j) {
-                    tmem_st_32x32b_x4(sfa_col + lane_base + 4 * j, *reinterpret_cast<const uint4*>(sfa + 512 * j));
 #pragma unroll
-                    for (int h = 0; h < C::kBHalves; ++h)
-                        tmem_st_32x32b_x4(sfb_col + lane_base + 4 * (C::kBHalves * j + h),
-                                          *reinterpret_cast<const uint4*>(sfb + 512 * (h * C::kAtomsK + j)));
+                for (int j = 0; j < C::kAtomsK; ++j) {
+                    if (j < atoms) {
+                        tmem_st_32x32b_x4(sfa_col + lane_base + 4 * j, *reinterpret_cast<const uint4*>(sfa + 512 * j));
+#pragma unroll
+                        for (int h = 0; h < C::kBHalves; ++h)
+                            tmem_st_32x32b_x4(sfb_col + lane_base + 4 * (C::kBHalves * j + h),
+                                              *reinterpret_cast<const uint4*>(sfb + 512 * (h * C::kAtomsK + j)));
+                    }
                 }
                 tmem_st_wait();
                 tc_fence_before();
@@ -318,10 +326,45 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) mbar_arrive(&sf_ready[s]);
             }
         }
+    } else if (warp == kScaleLoadWarp) {
+        // ------------------------------------------------ block-scale loader
+        // The 512-byte 128x4 scale tiles of A and B for each stage, into the
+        // stage's scale slots, completing on sf_full (same ring and empty
+        // barriers as the A/B tiles).
+        if (lane == 0) {
+            uint32_t it = 0, n_armed = 0;
+            for (int t = blockIdx.x; t < total; t += gridDim.x) {
+                const Tile tl = decode<BN, C::kStageK>(args, t);
+                for (int kb = 0; kb < tl.num_kb; ++kb, ++it) {
+                    const int s = it % C::kStages;
+                    mbar_wait_flag(&empty[s], ((it / C::kStages) & 1) ^ 1, abort_flag);
+                    const uint32_t live = live_flag(abort_flag);
+                    const int ka = tl.a_k0 + kb * C::kStageK, kbb = tl.b_k0 + kb * C::kStageK;
+                    const int left = tl.k_len - kb * C::kStageK;
+                    const int atoms = min(C::kAtomsK, (left + C::kElemPerAtom - 1) / C::kElemPerAtom);
+                    const uint32_t sf_bytes = (uint32_t)atoms * 512u;
+                    mbar_arrive_expect_tx_if(&sf_full[s], sf_bytes * (1 + C::kBHalves), live);
+                    n_armed += live;
+                    bulk_load_if(smem + C::kSfa + s * C::kSfaBytes,
+                                 args.a_scale + ((int64_t)(tl.a_row / 128) * args.a_scale_ctiles + ka / C::kElemPerAtom) * 512,
+                                 sf_bytes, &sf_full[s], live);
+#pragma unroll
+                    for (int h = 0; h < C::kBHalves; ++h)
+                        bulk_load_if(smem + C::kSfb + s * C::kSfbBytes + h * C::kAtomsK * 512,
+                                     args.b_scale +
+                                         ((int64_t)(tl.b_row / 128 + h) * args.b_scale_ctiles + kbb / C::kElemPerAtom) * 512,
+                                     sf_bytes, &sf_full[s], live);
+                }
+            }
+            const uint32_t n = n_armed < (uint32_t)C::kStages ? n_armed : (uint32_t)C::kStages;
+            for (uint32_t i = 0; i < n; ++i) {
+                const uint32_t k = n_armed - 1 - i;
+                mbar_wait(&sf_full[k % C::kStages], (k / C::kStages) & 1, args.status);
+            }
+        }
     } else {
         // ------------------------------------------------ epilogue (warps 6..13)
         constexpr int kCols = BN / 2;       // columns per warp
-        constexpr int kPasses = kCols / 64;  // 64-column passes
         const int quad = warp & 3;
         const int half = (warp - kFirstEpiWarp) >> 2;
         const int r = quad * 32 + lane;     // tile row = TMEM lane
@@ -347,51 +390,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int col0 = tl.n_tile * BN + half * kCols;
             const int64_t rowoff = gr.c_off + (int64_t)out_row * args.ldc + col0;
             const uint32_t taddr = tmem_base + (uint32_t)(as * BN + half * kCols) + ((uint32_t)(quad * 32) << 16);
-#pragma unroll 1
-            for (int p = 0; p < kPasses; ++p) {
-                uint32_t v[64];
-                if (tl.num_kb > 0) {
-                    tmem_ld_32x32b_x32(taddr + (uint32_t)(p * 64), *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
-                    tmem_ld_32x32b_x32(taddr + (uint32_t)(p * 64 + 32), *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
-                    tmem_ld_wait();
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 64; ++i) v[i] = 0u;  // empty contraction: zero
-                }
-                if (p == kPasses - 1) {  // accumulator fully read: hand it back to the MMA warp
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&acc_empty[as]);
-                }
-                if (!row_ok) continue;
-#pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    const int cc = p * 64 + c * 32;  // column offset within this warp's slice
-                    float f[32];
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        float y = __fmul_rn(alpha, __uint_as_float(v[c * 32 + i]));
-                        if (args.bias) y = __fadd_rn(y, __uint_as_float((uint32_t)args.bias[col0 + cc + i] << 16));
-                        f[i] = y;
-                    }
-                    if (args.c_fp32) {
-                        float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(args.C) + rowoff + cc);
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) dst[i] = make_float4(f[4 * i], f[4 * i + 1], f[4 * i + 2], f[4 * i + 3]);
-                    } else {
-                        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(args.C) + rowoff + cc);
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            __nv_bfloat162 p0 = __floats2bfloat162_rn(f[8 * i + 0], f[8 * i + 1]);
-                            __nv_bfloat162 p1 = __floats2bfloat162_rn(f[8 * i + 2], f[8 * i + 3]);
-                            __nv_bfloat162 p2 = __floats2bfloat162_rn(f[8 * i + 4], f[8 * i + 5]);
-                            __nv_bfloat162 p3 = __floats2bfloat162_rn(f[8 * i + 6], f[8 * i + 7]);
-                            dst[i] = make_uint4(*reinterpret_cast<uint32_t*>(&p0), *reinterpret_cast<uint32_t*>(&p1),
-                                                *reinterpret_cast<uint32_t*>(&p2), *reinterpret_cast<uint32_t*>(&p3));
-                        }
-                    }
-                }
-            }
+            epilogue_slice<kCols>(args, taddr, tl.num_kb > 0, alpha, col0, rowoff, row_ok, [&] {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&acc_empty[as]);
+            });
         }
     }
 

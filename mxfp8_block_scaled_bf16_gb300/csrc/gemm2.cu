@@ -29,6 +29,7 @@
 // MMAs, copies or arrivals may still reach it.
 #include <cuda.h>
 
+#include "gemm_epilogue.cuh"
 #include "nvq_device.cuh"
 #include "nvq_kernels.h"
 
@@ -108,11 +109,11 @@ __device__ __forceinline__ PairTile decode(const GemmArgs& a, int t, uint32_t ra
     PairTile r;
     const int mp = t / a.n_tiles;
     r.n_tile = t - mp * a.n_tiles;
-    int lo = 0, hi = a.G - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (a.groups[mid].pm_tile0 <= mp) lo = mid;
-        else hi = mid - 1;
+    int lo = 0;  // last group whose first pair tile <= mp (fixed-length branchless search)
+#pragma unroll
+    for (int step = kMaxGroups / 2; step >= 1; step >>= 1) {
+        const int mid = lo + step;
+        lo = (mid < a.G && a.groups[mid].pm_tile0 <= mp) ? mid : lo;
     }
     const GemmGroup& gr = a.groups[lo];
     r.g = lo;
@@ -202,44 +203,45 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer (both CTAs)
+        // Straight-line issue as in gemm.cu: PTX-loop waits, copies guarded by
+        // the CTA's live flag.
         if (lane == 0) {
-            uint32_t it = 0;
-            bool ok = true;
-            for (int t = pair; t < total && ok; t += n_pairs) {
+            uint32_t it = 0, n_armed = 0;
+            const uint32_t leader = rank == 0 ? 1u : 0u;
+            for (int t = pair; t < total; t += n_pairs) {
                 const PairTile tl = decode<C::kStageK>(args, t, rank);
                 for (int kb = 0; kb < tl.num_kb; ++kb, ++it) {
                     const int s = it % C::kStages;
-                    if (!wait_or_abort(&empty[s], ((it / C::kStages) & 1) ^ 1, args.status, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
+                    mbar_wait_flag(&empty[s], ((it / C::kStages) & 1) ^ 1, abort_flag);
+                    const uint32_t live = live_flag(abort_flag);
                     const int ka = tl.a_k0 + kb * C::kStageK, kbb = tl.b_k0 + kb * C::kStageK;
                     const int left = tl.k_len - kb * C::kStageK;
                     const int atoms = min(C::kAtomsK, (left + C::kElemPerAtom - 1) / C::kElemPerAtom);
                     const uint32_t sf_bytes = (uint32_t)atoms * 512u;
-                    if (rank == 0) mbar_arrive_expect_tx(&full[s], 4u * kHalfTileBytes);  // A + B of both CTAs
-                    mbar_arrive_expect_tx(&sf_full[s], sf_bytes * (1 + C::kSfbHalves));
+                    mbar_arrive_expect_tx_if(&full[s], 4u * kHalfTileBytes, live & leader);  // A + B of both CTAs
+                    mbar_arrive_expect_tx_if(&sf_full[s], sf_bytes * (1 + C::kSfbHalves), live);
+                    n_armed += live;
                     const uint32_t bar = map_to_rank(&full[s], 0);
                     const int b_row = tl.b_row_pair + (int)rank * 128;
-                    tma_load_2d_pair(smem + C::kA + s * kHalfTileBytes, &a_map, bar, FMT == 1 ? ka / 2 : ka, tl.a_row);
-                    tma_load_2d_pair(smem + C::kB + s * kHalfTileBytes, &b_map, bar, FMT == 1 ? kbb / 2 : kbb, b_row);
-                    bulk_load(smem + C::kSfa + s * C::kSfaBytes,
-                              args.a_scale + ((int64_t)(tl.a_row / 128) * args.a_scale_ctiles + ka / C::kElemPerAtom) * 512,
-                              sf_bytes, &sf_full[s]);
+                    tma_load_2d_pair_if(smem + C::kA + s * kHalfTileBytes, &a_map, bar, FMT == 1 ? ka / 2 : ka, tl.a_row, live);
+                    tma_load_2d_pair_if(smem + C::kB + s * kHalfTileBytes, &b_map, bar, FMT == 1 ? kbb / 2 : kbb, b_row, live);
+                    bulk_load_if(smem + C::kSfa + s * C::kSfaBytes,
+                                 args.a_scale + ((int64_t)(tl.a_row / 128) * args.a_scale_ctiles + ka / C::kElemPerAtom) * 512,
+                                 sf_bytes, &sf_full[s], live);
 #pragma unroll
                     for (int h = 0; h < C::kSfbHalves; ++h) {
                         const int brow = SFB_FULL ? tl.b_row_pair + h * 128 : b_row;
-                        bulk_load(smem + C::kSfb + s * C::kSfbBytes + h * C::kAtomsK * 512,
-                                  args.b_scale + ((int64_t)(brow / 128) * args.b_scale_ctiles + kbb / C::kElemPerAtom) * 512,
-                                  sf_bytes, &sf_full[s]);
+                        bulk_load_if(smem + C::kSfb + s * C::kSfbBytes + h * C::kAtomsK * 512,
+                                     args.b_scale + ((int64_t)(brow / 128) * args.b_scale_ctiles + kbb / C::kElemPerAtom) * 512,
+                                     sf_bytes, &sf_full[s], live);
                     }
                 }
             }
             // drain this CTA's scale copies; the leader also drains the A/B
             // copies of both CTAs (they complete on its full barriers)
-            const uint32_t n = it < (uint32_t)C::kStages ? it : (uint32_t)C::kStages;
+            const uint32_t n = n_armed < (uint32_t)C::kStages ? n_armed : (uint32_t)C::kStages;
             for (uint32_t i = 0; i < n; ++i) {
-                const uint32_t k = it - 1 - i;
+                const uint32_t k = n_armed - 1 - i;
                 mbar_wait(&sf_full[k % C::kStages], (k / C::kStages) & 1, args.status);
                 if (rank == 0) mbar_wait(&full[k % C::kStages], (k / C::kStages) & 1, args.status);
             }
@@ -247,43 +249,44 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer (leader CTA)
         if (lane == 0 && rank == 0) {
+            constexpr int kMmas = C::kStageK / C::kMmaK;
+            const uint64_t a_desc0 = smem_desc(smem_u32(smem + C::kA), 16, 1024, kSwizzle128B);
+            const uint64_t b_desc0 = smem_desc(smem_u32(smem + C::kB), 16, 1024, kSwizzle128B);
             uint32_t it = 0, tl_i = 0;
-            bool ok = true;
-            for (int t = pair; t < total && ok; t += n_pairs, ++tl_i) {
+            for (int t = pair; t < total; t += n_pairs, ++tl_i) {
                 const PairTile tl = decode<C::kStageK>(args, t, 0);
-                if (!wait_or_abort(acc_empty, (tl_i & 1) ^ 1, args.status, abort_flag)) break;
+                mbar_wait_flag(acc_empty, (tl_i & 1) ^ 1, abort_flag);
                 tc_fence_after();
                 for (int kb = 0; kb < tl.num_kb; ++kb, ++it) {
                     const int s = it % C::kStages;
                     const uint32_t par = (it / C::kStages) & 1;
-                    if (!wait_or_abort(&full[s], par, args.status, abort_flag) ||
-                        !wait_or_abort(&sf_ready[s], par, args.status, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
+                    mbar_wait_flag(&full[s], par, abort_flag);
+                    mbar_wait_flag(&sf_ready[s], par, abort_flag);
                     tc_fence_after();
-                    const int left = tl.k_len - kb * C::kStageK;
-                    const int n_mma = min(C::kStageK, left) / C::kMmaK;
+                    const uint32_t live = live_flag(abort_flag);
+                    const int n_mma = min(C::kStageK, tl.k_len - kb * C::kStageK) / C::kMmaK;
                     const uint32_t sfa_col = tmem_base + C::kSfCol0 + (uint32_t)s * C::kSfColsPerStage;
                     const uint32_t sfb_col = sfa_col + C::kSfaCols;
-                    const uint32_t a_smem = smem_u32(smem + C::kA + s * kHalfTileBytes);
-                    const uint32_t b_smem = smem_u32(smem + C::kB + s * kHalfTileBytes);
-                    for (int j = 0; j < n_mma; ++j) {
-                        const uint64_t ad = smem_desc(a_smem + 32 * j, 16, 1024, kSwizzle128B);
-                        const uint64_t bd = smem_desc(b_smem + 32 * j, 16, 1024, kSwizzle128B);
+                    const uint64_t ad = a_desc0 + (uint64_t)((s * kHalfTileBytes) >> 4);
+                    const uint64_t bd = b_desc0 + (uint64_t)((s * kHalfTileBytes) >> 4);
+#pragma unroll
+                    for (int j = 0; j < kMmas; ++j) {
+                        const uint32_t on = (j < n_mma) ? live : 0u;
                         const uint32_t acc = (kb > 0 || j > 0) ? 1u : 0u;
                         if constexpr (FMT == 1)
-                            tc_mma_nvf4_pair(tmem_base, ad, bd, make_idesc<1>(0), sfa_col + 4 * j,
-                                             sfb_col + 4 * C::kSfbHalves * j, acc);
+                            tc_mma_nvf4_pair_if(tmem_base, ad + 2 * j, bd + 2 * j, make_idesc<1>(0), sfa_col + 4 * j,
+                                                sfb_col + 4 * C::kSfbHalves * j, acc, on);
                         else
-                            tc_mma_mxf8_pair(tmem_base, ad, bd, make_idesc<2>((uint32_t)j), sfa_col, sfb_col, acc);
+                            tc_mma_mxf8_pair_if(tmem_base, ad + 2 * j, bd + 2 * j, make_idesc<2>((uint32_t)j), sfa_col,
+                                                sfb_col, acc, on);
                     }
-                    tc_commit_pair(&empty[s], 0x3);
+                    tc_commit_pair_if(&empty[s], 0x3, live);
                 }
-                tc_commit_pair(acc_full, 0x3);
+                tc_commit_pair_if(acc_full, 0x3, live_flag(abort_flag));
             }
             tc_commit_pair(mma_done, 0x1);
             mbar_wait(mma_done, 0, args.status);
+            if (*abort_flag) record_error(args.status, kErrTimeout);
         }
     } else if (warp < kFirstEpiWarp) {
         // ------------------------------------------------ scale staging (both CTAs)
@@ -325,7 +328,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     } else {
         // ------------------------------------------------ epilogue (both CTAs)
         constexpr int kCols = BN / 2;
-        constexpr int kPasses = kCols / 64;
         const int quad = warp & 3;
         const int half = (warp - kFirstEpiWarp) >> 2;
         const int r = quad * 32 + lane;
@@ -349,51 +351,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const int col0 = tl.n_tile * BN + half * kCols;
             const int64_t rowoff = gr.c_off + (int64_t)out_row * args.ldc + col0;
             const uint32_t taddr = tmem_base + (uint32_t)(half * kCols) + ((uint32_t)(quad * 32) << 16);
-#pragma unroll 1
-            for (int p = 0; p < kPasses; ++p) {
-                uint32_t v[64];
-                if (tl.num_kb > 0) {
-                    tmem_ld_32x32b_x32(taddr + (uint32_t)(p * 64), *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
-                    tmem_ld_32x32b_x32(taddr + (uint32_t)(p * 64 + 32), *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
-                    tmem_ld_wait();
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 64; ++i) v[i] = 0u;
-                }
-                if (p == kPasses - 1) {
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) arrive_leader(acc_empty, rank);
-                }
-                if (!row_ok) continue;
-#pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    const int cc = p * 64 + c * 32;
-                    float f[32];
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        float y = __fmul_rn(alpha, __uint_as_float(v[c * 32 + i]));
-                        if (args.bias) y = __fadd_rn(y, __uint_as_float((uint32_t)args.bias[col0 + cc + i] << 16));
-                        f[i] = y;
-                    }
-                    if (args.c_fp32) {
-                        float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(args.C) + rowoff + cc);
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) dst[i] = make_float4(f[4 * i], f[4 * i + 1], f[4 * i + 2], f[4 * i + 3]);
-                    } else {
-                        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(args.C) + rowoff + cc);
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            __nv_bfloat162 p0 = __floats2bfloat162_rn(f[8 * i + 0], f[8 * i + 1]);
-                            __nv_bfloat162 p1 = __floats2bfloat162_rn(f[8 * i + 2], f[8 * i + 3]);
-                            __nv_bfloat162 p2 = __floats2bfloat162_rn(f[8 * i + 4], f[8 * i + 5]);
-                            __nv_bfloat162 p3 = __floats2bfloat162_rn(f[8 * i + 6], f[8 * i + 7]);
-                            dst[i] = make_uint4(*reinterpret_cast<uint32_t*>(&p0), *reinterpret_cast<uint32_t*>(&p1),
-                                                *reinterpret_cast<uint32_t*>(&p2), *reinterpret_cast<uint32_t*>(&p3));
-                        }
-                    }
-                }
-            }
+            epilogue_slice<kCols>(args, taddr, tl.num_kb > 0, alpha, col0, rowoff, row_ok, [&] {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) arrive_leader(acc_empty, rank);
+            });
         }
     }
 

@@ -1,0 +1,90 @@
+// gemm_epilogue.cuh -- the accumulator epilogue shared by the single-CTA and
+// CTA-pair GEMM kernels: one warp turns its TMEM slice (32 accumulator rows,
+// kCols fp32 columns) into C = alpha * acc (+ bias) rows.
+#pragma once
+
+#include "nvq_device.cuh"
+#include "nvq_kernels.h"
+
+namespace nvq {
+
+// taddr: TMEM address of the warp's slice (its lane quadrant, first column);
+// have_k: false for an empty contraction (the slice is zero); rowoff: element
+// offset of the row's first column in C; release(): hands the accumulator
+// back to the MMA issuer once every TMEM load of the slice has completed.
+template <int kCols, typename Release>
+__device__ __forceinline__ void epilogue_slice(const GemmArgs& args, uint32_t taddr, bool have_k, float alpha,
+                                               int col0, int64_t rowoff, bool row_ok, Release release)
+{
+    static_assert(kCols % 64 == 0, "64-column granularity");
+    if (!args.c_fp32) {
+        // bf16: read the whole slice in 32-column chunks, scale, add the bias
+        // and pack in registers, release the accumulator, then store -- the
+        // next tile's MMAs overlap the global stores.
+        uint32_t packed[kCols / 2];
+#pragma unroll
+        for (int c = 0; c < kCols / 32; ++c) {
+            uint32_t v[32];
+            if (have_k) {
+                tmem_ld_32x32b_x32(taddr + (uint32_t)(c * 32), v);
+                tmem_ld_wait();
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = 0u;
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                float y0 = __fmul_rn(alpha, __uint_as_float(v[2 * i]));
+                float y1 = __fmul_rn(alpha, __uint_as_float(v[2 * i + 1]));
+                if (args.bias) {
+                    y0 = __fadd_rn(y0, __uint_as_float((uint32_t)args.bias[col0 + c * 32 + 2 * i] << 16));
+                    y1 = __fadd_rn(y1, __uint_as_float((uint32_t)args.bias[col0 + c * 32 + 2 * i + 1] << 16));
+                }
+                __nv_bfloat162 b2 = __floats2bfloat162_rn(y0, y1);
+                packed[c * 16 + i] = *reinterpret_cast<uint32_t*>(&b2);
+            }
+        }
+        release();
+        if (!row_ok) return;
+        if (args.c_st32) {  // 32-byte stores, one full L2 sector each
+            uint16_t* dst = reinterpret_cast<uint16_t*>(args.C) + rowoff;
+#pragma unroll
+            for (int i = 0; i < kCols / 16; ++i) st_global_v8(dst + 16 * i, &packed[8 * i]);
+        } else {
+            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(args.C) + rowoff);
+#pragma unroll
+            for (int i = 0; i < kCols / 8; ++i)
+                dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+        }
+        return;
+    }
+    // fp32: 64-column passes, the accumulator released after the last load
+#pragma unroll 1
+    for (int p = 0; p < kCols / 64; ++p) {
+        uint32_t v[64];
+        if (have_k) {
+            tmem_ld_32x32b_x32(taddr + (uint32_t)(p * 64), *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+            tmem_ld_32x32b_x32(taddr + (uint32_t)(p * 64 + 32), *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+            tmem_ld_wait();
+        } else {
+#pragma unroll
+            for (int i = 0; i < 64; ++i) v[i] = 0u;
+        }
+        if (p == kCols / 64 - 1) release();
+        if (!row_ok) continue;
+        float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(args.C) + rowoff + p * 64);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            float f[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                float y = __fmul_rn(alpha, __uint_as_float(v[4 * i + e]));
+                if (args.bias) y = __fadd_rn(y, __uint_as_float((uint32_t)args.bias[col0 + p * 64 + 4 * i + e] << 16));
+                f[e] = y;
+            }
+            dst[i] = make_float4(f[0], f[1], f[2], f[3]);
+        }
+    }
+}
+
+}  // namespace nvq

@@ -94,6 +94,49 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* s
     }
 }
 
+// Bounded wait whose whole polling loop is PTX, so no value flows back into
+// the caller's control flow: the issuing loops of the GEMM's producer and MMA
+// threads stay free of data-dependent branches, which on this part slowed
+// tensor-core and TMA issue (a loop around tcgen05.mma issue measured ~1.5x
+// slower than straight-line issue).  Returns when the phase completes, when
+// *abort_flag is already set, or after kWaitLimitNs, in which case it sets
+// *abort_flag itself; callers read the flag afterwards (a "live" predicate)
+// and guard their async work with it.
+__device__ __forceinline__ void mbar_wait_flag(uint64_t* bar, uint32_t parity, volatile int* abort_flag)
+{
+    asm volatile(
+        "{\n\t.reg .pred P1;\n\t.reg .b64 t0, t1;\n\t.reg .b32 ab;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 P1, [%0], %1;\n\t"
+        "@P1 bra.uni DONE;\n\t"
+        "mov.u64 t0, %%globaltimer;\n\t"
+        "LOOP:\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 P1, [%0], %1;\n\t"
+        "@P1 bra.uni DONE;\n\t"
+        "ld.volatile.shared.u32 ab, [%2];\n\t"
+        "setp.ne.u32 P1, ab, 0;\n\t"
+        "@P1 bra.uni DONE;\n\t"
+        "mov.u64 t1, %%globaltimer;\n\t"
+        "sub.u64 t1, t1, t0;\n\t"
+        "setp.lt.u64 P1, t1, %3;\n\t"
+        "@P1 bra.uni LOOP;\n\t"
+        "st.volatile.shared.u32 [%2], 1;\n\t"
+        "DONE:\n\t}" ::"r"(smem_u32(bar)),
+        "r"(parity), "r"(smem_u32(const_cast<int*>(abort_flag))), "l"(kWaitLimitNs)
+        : "memory");
+}
+
+// 1 while the CTA has not aborted (read after a mbar_wait_flag).
+__device__ __forceinline__ uint32_t live_flag(volatile int* abort_flag) { return *abort_flag == 0 ? 1u : 0u; }
+
+__device__ __forceinline__ void mbar_arrive_expect_tx_if(uint64_t* bar, uint32_t bytes, uint32_t live)
+{
+    asm volatile(
+        "{\n\t.reg .pred g;\n\tsetp.ne.b32 g, %2, 0;\n\t"
+        "@g mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n\t}" ::"r"(smem_u32(bar)),
+        "r"(bytes), "r"(live)
+        : "memory");
+}
+
 // ------------------------------------------------------------------ TMA
 __device__ __forceinline__ void tma_prefetch_desc(const void* desc)
 {
@@ -118,6 +161,28 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
             smem_u32(dst)),
         "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// tma_load_2d / bulk_load issued only when live != 0.
+__device__ __forceinline__ void tma_load_2d_if(void* dst, const void* desc, uint64_t* bar, int32_t x, int32_t y,
+                                               uint32_t live)
+{
+    asm volatile(
+        "{\n\t.reg .pred g;\n\tsetp.ne.b32 g, %5, 0;\n\t"
+        "@g cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];\n\t}" ::"r"(smem_u32(dst)),
+        "l"(desc), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(live)
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_load_if(void* dst, const void* src, uint32_t bytes, uint64_t* bar, uint32_t live)
+{
+    asm volatile(
+        "{\n\t.reg .pred g;\n\tsetp.ne.b32 g, %4, 0;\n\t"
+        "@g cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n\t}" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar)), "r"(live)
         : "memory");
 }
 
@@ -150,6 +215,15 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar)
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                      smem_u32(bar))
                  : "memory");
+}
+
+__device__ __forceinline__ void tc_commit_if(uint64_t* bar, uint32_t live)
+{
+    asm volatile(
+        "{\n\t.reg .pred g;\n\tsetp.ne.b32 g, %1, 0;\n\t"
+        "@g tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(smem_u32(bar)),
+        "r"(live)
+        : "memory");
 }
 
 // Shared-memory matrix descriptor (tcgen05): start, leading/stride byte
@@ -186,6 +260,36 @@ __device__ __forceinline__ void tc_mma_nvf4(uint32_t d_tmem, uint64_t a_desc, ui
         "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X"
         " [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+// tc_mma_nvf4 issued only when live != 0.
+__device__ __forceinline__ void tc_mma_nvf4_if(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                               uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate,
+                                               uint32_t live)
+{
+    asm volatile(
+        "{\n\t.reg .pred p, g;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "setp.ne.b32 g, %7, 0;\n\t"
+        "@g tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X"
+        " [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate), "r"(live)
+        : "memory");
+}
+
+// tc_mma_mxf8 issued only when live != 0.
+__device__ __forceinline__ void tc_mma_mxf8_if(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                               uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate,
+                                               uint32_t live)
+{
+    asm volatile(
+        "{\n\t.reg .pred p, g;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "setp.ne.b32 g, %7, 0;\n\t"
+        "@g tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X"
+        " [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate), "r"(live)
         : "memory");
 }
 
@@ -289,6 +393,18 @@ __device__ __forceinline__ void tma_load_2d_pair(void* dst, const void* desc, ui
         : "memory");
 }
 
+// tma_load_2d_pair issued only when live != 0.
+__device__ __forceinline__ void tma_load_2d_pair_if(void* dst, const void* desc, uint32_t bar_cluster_addr, int32_t x,
+                                                    int32_t y, uint32_t live)
+{
+    asm volatile(
+        "{\n\t.reg .pred g;\n\tsetp.ne.b32 g, %5, 0;\n\t"
+        "@g cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];\n\t}" ::"r"(smem_u32(dst)),
+        "l"(desc), "r"(bar_cluster_addr), "r"(x), "r"(y), "r"(live)
+        : "memory");
+}
+
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t* dst_smem, uint32_t ncols)
 {
     asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
@@ -317,6 +433,46 @@ __device__ __forceinline__ void tc_commit_pair(uint64_t* bar, uint16_t mask)
         : "memory");
 }
 
+// tc_commit_pair issued only when live != 0.
+__device__ __forceinline__ void tc_commit_pair_if(uint64_t* bar, uint16_t mask, uint32_t live)
+{
+    asm volatile(
+        "{\n\t.reg .pred g;\n\tsetp.ne.b32 g, %2, 0;\n\t"
+        "@g tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n\t}" ::"r"(
+            smem_u32(bar)),
+        "h"(mask), "r"(live)
+        : "memory");
+}
+
+// Pair MMAs issued only when live != 0.
+__device__ __forceinline__ void tc_mma_nvf4_pair_if(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                                    uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate,
+                                                    uint32_t live)
+{
+    asm volatile(
+        "{\n\t.reg .pred p, g;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "setp.ne.b32 g, %7, 0;\n\t"
+        "@g tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X"
+        " [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate), "r"(live)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_mma_mxf8_pair_if(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                                    uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate,
+                                                    uint32_t live)
+{
+    asm volatile(
+        "{\n\t.reg .pred p, g;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "setp.ne.b32 g, %7, 0;\n\t"
+        "@g tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X"
+        " [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate), "r"(live)
+        : "memory");
+}
+
 __device__ __forceinline__ void tc_mma_nvf4_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                                  uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate)
 {
@@ -339,6 +495,14 @@ __device__ __forceinline__ void tc_mma_mxf8_pair(uint32_t d_tmem, uint64_t a_des
         " [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
         : "memory");
+}
+
+// 32-byte global store (256-bit vector; the address must be 32-byte aligned).
+__device__ __forceinline__ void st_global_v8(void* dst, const uint32_t* w)
+{
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(w[0]), "r"(w[1]),
+                 "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                 : "memory");
 }
 
 // ------------------------------------------------------------------ formats

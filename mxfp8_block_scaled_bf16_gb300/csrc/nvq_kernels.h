@@ -87,6 +87,7 @@ struct GemmArgs {
     void* C;
     int64_t ldc;
     int c_fp32;
+    int c_st32;  // bf16 C, base and row pitch 32-byte aligned: 32-byte stores
     int* status;           // device status word
     int debug_drop_first_load;  // test hook: arm stage 0's barrier but issue no copy
     GemmGroup groups[kMaxGroups];
