@@ -19,12 +19,16 @@
 //               (NVFP4: kind::mxf4nvf4 scale_vec::4X, K = 64; MXFP8:
 //               kind::mxf8f6f4 scale_vec::1X, K = 32, the scale byte chosen by
 //               the scale-factor id) into one of the TMEM accumulator stages;
-//   warps 2..5  scale staging: each 128x4 scale tile goes to TMEM in the
-//               replicated layout the block-scaled MMA reads (every lane
-//               quadrant holds the tile's 32 16-byte rows); warp w writes its
-//               quadrant w % 4 with tcgen05.st (the smem->TMEM tcgen05.cp path
-//               runs in the MMA's in-order pipe, where it cost more than the
-//               MMAs themselves);
+//   warps 2..5  scale staging into TMEM with tcgen05.st, warp w writing lane
+//               quadrant q = w % 4 (the smem->TMEM tcgen05.cp path runs in the
+//               MMA's in-order pipe, where it cost more than the MMAs
+//               themselves).  A 128x4 scale tile is 32 rows of 16 bytes, row l
+//               holding tile rows l, l+32, l+64, l+96.  The MMA reads the A
+//               scales of rows 32q..32q+31 from quadrant q, column base + q, so
+//               warp q writes only word q of each row there; every quadrant
+//               reads the B scales of all N columns, so each gets the whole
+//               16-byte rows (4 columns per tile) -- both found by testing
+//               layouts against the exact results;
 //   warps 6..13 epilogue: warp w reads TMEM lane quadrant w % 4, half
 //               (w - 6) / 4 of the columns; after its last load it releases the
 //               accumulator to the MMA warp, then stores the scaled (+ bias)
@@ -283,11 +287,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------ scale staging (warps 2..5)
         // A 512-byte 128x4 scale tile is 32 rows of 16 bytes; row l holds tile
         // rows l, l+32, l+64, l+96 (one 32-bit word each: the scales of the
-        // tile's four k-steps).  The MMA of lane quadrant q reads word q of
-        // row l from TMEM lane 32 q + l; warp w writes the whole 16-byte row l
-        // into lane l of its quadrant w % 4 (4 columns, tcgen05.st), which is
-        // the layout a replicating smem->TMEM copy produces, without the MMA
-        // pipe.
+        // tile's four 16- or 32-element k-blocks).  A scales: the MMA of lane
+        // quadrant q reads word q of row l from TMEM lane 32 q + l, column
+        // base + q.  B scales: every quadrant reads all of them, so warp q
+        // writes the whole 16-byte row l into lane l of its quadrant (4
+        // columns), the layout a replicating smem->TMEM copy produces.
         const int q = warp & 3;
         uint32_t it = 0;
         bool ok = true;
@@ -313,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int j = 0; j < C::kAtomsK; ++j) {
                     if (j < atoms) {
-                        tmem_st_32x32b_x4(sfa_col + lane_base + 4 * j, *reinterpret_cast<const uint4*>(sfa + 512 * j));
+                        tmem_st_32x32b_x1(sfa_col + lane_base + 4 * j + q, *reinterpret_cast<const uint32_t*>(sfa + 512 * j + 4 * q));
 #pragma unroll
                         for (int h = 0; h < C::kBHalves; ++h)
                             tmem_st_32x32b_x4(sfb_col + lane_base + 4 * (C::kBHalves * j + h),

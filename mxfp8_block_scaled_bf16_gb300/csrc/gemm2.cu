@@ -313,7 +313,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 const uint8_t* sfa = smem + C::kSfa + s * C::kSfaBytes + lane * 16;
                 const uint8_t* sfb = smem + C::kSfb + s * C::kSfbBytes + lane * 16;
                 for (int j = 0; j < atoms; ++j) {
-                    tmem_st_32x32b_x4(sfa_col + lane_base + 4 * j, *reinterpret_cast<const uint4*>(sfa + 512 * j));
+                    tmem_st_32x32b_x1(sfa_col + lane_base + 4 * j + q, *reinterpret_cast<const uint32_t*>(sfa + 512 * j + 4 * q));
 #pragma unroll
                     for (int h = 0; h < C::kSfbHalves; ++h)
                         tmem_st_32x32b_x4(sfb_col + lane_base + 4 * (C::kSfbHalves * j + h),
