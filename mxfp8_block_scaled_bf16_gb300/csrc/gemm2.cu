@@ -43,7 +43,8 @@ constexpr int kHalfTileBytes = 128 * 128;
 constexpr int kScaleWarps = 4;
 constexpr int kEpiWarps = 8;
 constexpr int kFirstEpiWarp = 2 + kScaleWarps;
-constexpr int kThreads = 32 * (kFirstEpiWarp + kEpiWarps);
+constexpr int kScaleLoadWarp = kFirstEpiWarp + kEpiWarps;  // block-scale copies
+constexpr int kThreads = 32 * (kScaleLoadWarp + 1);
 constexpr uint32_t kTmemCols = 512;
 
 // SFB_FULL: each CTA's TMEM holds the B scales of all 256 columns (both
@@ -215,34 +216,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     mbar_wait_flag(&empty[s], ((it / C::kStages) & 1) ^ 1, abort_flag);
                     const uint32_t live = live_flag(abort_flag);
                     const int ka = tl.a_k0 + kb * C::kStageK, kbb = tl.b_k0 + kb * C::kStageK;
-                    const int left = tl.k_len - kb * C::kStageK;
-                    const int atoms = min(C::kAtomsK, (left + C::kElemPerAtom - 1) / C::kElemPerAtom);
-                    const uint32_t sf_bytes = (uint32_t)atoms * 512u;
                     mbar_arrive_expect_tx_if(&full[s], 4u * kHalfTileBytes, live & leader);  // A + B of both CTAs
-                    mbar_arrive_expect_tx_if(&sf_full[s], sf_bytes * (1 + C::kSfbHalves), live);
                     n_armed += live;
                     const uint32_t bar = map_to_rank(&full[s], 0);
                     const int b_row = tl.b_row_pair + (int)rank * 128;
                     tma_load_2d_pair_if(smem + C::kA + s * kHalfTileBytes, &a_map, bar, FMT == 1 ? ka / 2 : ka, tl.a_row, live);
                     tma_load_2d_pair_if(smem + C::kB + s * kHalfTileBytes, &b_map, bar, FMT == 1 ? kbb / 2 : kbb, b_row, live);
-                    bulk_load_if(smem + C::kSfa + s * C::kSfaBytes,
-                                 args.a_scale + ((int64_t)(tl.a_row / 128) * args.a_scale_ctiles + ka / C::kElemPerAtom) * 512,
-                                 sf_bytes, &sf_full[s], live);
-#pragma unroll
-                    for (int h = 0; h < C::kSfbHalves; ++h) {
-                        const int brow = SFB_FULL ? tl.b_row_pair + h * 128 : b_row;
-                        bulk_load_if(smem + C::kSfb + s * C::kSfbBytes + h * C::kAtomsK * 512,
-                                     args.b_scale + ((int64_t)(brow / 128) * args.b_scale_ctiles + kbb / C::kElemPerAtom) * 512,
-                                     sf_bytes, &sf_full[s], live);
-                    }
                 }
             }
-            // drain this CTA's scale copies; the leader also drains the A/B
-            // copies of both CTAs (they complete on its full barriers)
+            // the leader drains the A/B copies of both CTAs (they complete on its full barriers)
             const uint32_t n = n_armed < (uint32_t)C::kStages ? n_armed : (uint32_t)C::kStages;
             for (uint32_t i = 0; i < n; ++i) {
                 const uint32_t k = n_armed - 1 - i;
-                mbar_wait(&sf_full[k % C::kStages], (k / C::kStages) & 1, args.status);
                 if (rank == 0) mbar_wait(&full[k % C::kStages], (k / C::kStages) & 1, args.status);
             }
         }
@@ -312,17 +297,57 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 const uint32_t lane_base = (uint32_t)(q * 32) << 16;
                 const uint8_t* sfa = smem + C::kSfa + s * C::kSfaBytes + lane * 16;
                 const uint8_t* sfb = smem + C::kSfb + s * C::kSfbBytes + lane * 16;
-                for (int j = 0; j < atoms; ++j) {
-                    tmem_st_32x32b_x1(sfa_col + lane_base + 4 * j + q, *reinterpret_cast<const uint32_t*>(sfa + 512 * j + 4 * q));
 #pragma unroll
-                    for (int h = 0; h < C::kSfbHalves; ++h)
-                        tmem_st_32x32b_x4(sfb_col + lane_base + 4 * (C::kSfbHalves * j + h),
-                                          *reinterpret_cast<const uint4*>(sfb + 512 * (h * C::kAtomsK + j)));
+                for (int j = 0; j < C::kAtomsK; ++j) {
+                    if (j < atoms) {
+                        tmem_st_32x32b_x1(sfa_col + lane_base + 4 * j + q, *reinterpret_cast<const uint32_t*>(sfa + 512 * j + 4 * q));
+#pragma unroll
+                        for (int h = 0; h < C::kSfbHalves; ++h)
+                            tmem_st_32x32b_x4(sfb_col + lane_base + 4 * (C::kSfbHalves * j + h),
+                                              *reinterpret_cast<const uint4*>(sfb + 512 * (h * C::kAtomsK + j)));
+                    }
                 }
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) arrive_leader(&sf_ready[s], rank);
+            }
+        }
+    } else if (warp == kScaleLoadWarp) {
+        // ------------------------------------------------ block-scale loader (both CTAs)
+        // This CTA's A scale tiles and the B scale tiles of all 256 columns,
+        // on its own thread (every copy costs its issuing thread ~100 cycles).
+        if (lane == 0) {
+            uint32_t it = 0, n_armed = 0;
+            for (int t = pair; t < total; t += n_pairs) {
+                const PairTile tl = decode<C::kStageK>(args, t, rank);
+                for (int kb = 0; kb < tl.num_kb; ++kb, ++it) {
+                    const int s = it % C::kStages;
+                    mbar_wait_flag(&empty[s], ((it / C::kStages) & 1) ^ 1, abort_flag);
+                    const uint32_t live = live_flag(abort_flag);
+                    const int ka = tl.a_k0 + kb * C::kStageK, kbb = tl.b_k0 + kb * C::kStageK;
+                    const int left = tl.k_len - kb * C::kStageK;
+                    const int atoms = min(C::kAtomsK, (left + C::kElemPerAtom - 1) / C::kElemPerAtom);
+                    const uint32_t sf_bytes = (uint32_t)atoms * 512u;
+                    mbar_arrive_expect_tx_if(&sf_full[s], sf_bytes * (1 + C::kSfbHalves), live);
+                    n_armed += live;
+                    const int b_row = tl.b_row_pair + (int)rank * 128;
+                    bulk_load_if(smem + C::kSfa + s * C::kSfaBytes,
+                                 args.a_scale + ((int64_t)(tl.a_row / 128) * args.a_scale_ctiles + ka / C::kElemPerAtom) * 512,
+                                 sf_bytes, &sf_full[s], live);
+#pragma unroll
+                    for (int h = 0; h < C::kSfbHalves; ++h) {
+                        const int brow = SFB_FULL ? tl.b_row_pair + h * 128 : b_row;
+                        bulk_load_if(smem + C::kSfb + s * C::kSfbBytes + h * C::kAtomsK * 512,
+                                     args.b_scale + ((int64_t)(brow / 128) * args.b_scale_ctiles + kbb / C::kElemPerAtom) * 512,
+                                     sf_bytes, &sf_full[s], live);
+                    }
+                }
+            }
+            const uint32_t n = n_armed < (uint32_t)C::kStages ? n_armed : (uint32_t)C::kStages;
+            for (uint32_t i = 0; i < n; ++i) {
+                const uint32_t k = n_armed - 1 - i;
+                mbar_wait(&sf_full[k % C::kStages], (k / C::kStages) & 1, args.status);
             }
         }
     } else {
