@@ -295,11 +295,8 @@ def run_ours(args, rank, world, local_rank):
         raise RuntimeError(f"device status {status} after the timed region")
 
     # whole-step device time, max over ranks
-    t = torch.tensor([ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms_max = float(t.item())
-    value = world * STEP_FLOP / (ms_max * 1e-3) / 1e12
+    ms_max = max_over_ranks(ms, world, dev)
+    value = job_rate(STEP_FLOP, world, ms_max) / 1e12
 
     # quantize-only throughput (x, W, dy: amax pass + fused row/col pass)
     q_ms = time_quantize(nvq, x, w, dy, sign, sr, fwd_bufs, bwd_bufs, stream)
@@ -354,6 +351,22 @@ def time_quantize(nvq, x, w, dy, sign, sr, fb, bb, stream, reps=5):
     t1.record(stream)
     torch.cuda.synchronize()
     return t0.elapsed_time(t1) / reps
+
+
+def max_over_ranks(ms: float, world: int, device="cpu") -> float:
+    """The job's step time: the slowest replica's (all-reduce MAX over ranks)."""
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(units_per_rank: float, world: int, ms_max: float) -> float:
+    """Whole-job throughput: every replica processes units_per_rank per step
+    (weak scaling), the job advances one step per ms_max."""
+    return world * units_per_rank / (ms_max * 1e-3)
 
 
 def measure_e2e(args, nvq, x_h, w_h, dy_h, sign, sr, dev, stream, world):
@@ -412,6 +425,9 @@ def measure_e2e(args, nvq, x_h, w_h, dy_h, sign, sr, dev, stream, world):
     for i in range(max(2, args.warmup)):
         step(i)
     torch.cuda.synchronize()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
     steps = max(2, min(args.steps, 10))
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
@@ -424,10 +440,10 @@ def measure_e2e(args, nvq, x_h, w_h, dy_h, sign, sr, dev, stream, world):
     s_in.wait_stream(s_comp)
     t1.record(s_in)
     torch.cuda.synchronize()
-    ms = t0.elapsed_time(t1) / steps
+    ms = max_over_ranks(t0.elapsed_time(t1) / steps, world, dev)
     bi = (M * K + N * K + M * N) * 2
     bo = (M * N + M * K + N * K) * 2
-    return {"value": world * STEP_FLOP / (ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": ms,
+    return {"value": job_rate(STEP_FLOP, world, ms) / 1e12, "unit": UNIT, "ms_per_step": ms,
             "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
             "api": "nvq_nvfp4_linear_fwd / _bwd_quantize / _dgrad / _wgrad with pinned host buffers; "
                    "copy-in, compute and copy-out streams over two buffer sets"}
@@ -672,6 +688,10 @@ def run_single_linear(args, nvq, inputs):
 
 
 def run_workload(args, rank, world, local_rank):
+    """The other configurations (quantize sweep, MoE grouped, Qwen3-8B stack,
+    single linear) are one-GPU measurements."""
+    if world > 1:
+        raise SystemExit(f"--workload {args.workload} runs on one GPU; the multi-GPU line is the default workload")
     import torch
     import __graft_entry__
     import mxfp8_block_scaled_bf16_gb300 as nvq
