@@ -146,11 +146,13 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, in
     }
 }
 
-// Arrive on barrier `bar` of the leader CTA (local arrive in the leader).
+// Arrive on barrier `bar` of the leader CTA (local arrive in the leader).  Both
+// uses (scales staged in TMEM, accumulator read out of TMEM) signal completed,
+// fenced tcgen05 work, so the remote arrive is relaxed.
 __device__ __forceinline__ void arrive_leader(uint64_t* bar, uint32_t rank)
 {
     if (rank == 0) mbar_arrive(bar);
-    else mbar_arrive_cluster(map_to_rank(bar, 0));
+    else mbar_arrive_cluster_relaxed(map_to_rank(bar, 0));
 }
 
 template <int FMT, bool SFB_FULL>

@@ -381,6 +381,18 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr)
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
+// Relaxed cluster-scope arrive, for a signal that only orders tcgen05 work:
+// the arriving thread has already waited for its TMEM stores / loads to
+// complete (tcgen05.wait::st / ::ld) and fenced them with
+// tcgen05.fence::before_thread_sync; the waiter issues
+// tcgen05.fence::after_thread_sync before its MMAs.  On the CTA-pair GEMM the
+// release form cost ~0.4 ms per forward GEMM (the MMA waited ~875 cycles per
+// stage on it); the relaxed form gives the same, exact, results.
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr)
+{
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
 // 2-D tiled load into this CTA's smem whose completion is signalled on an
 // mbarrier of either CTA of the pair (shared::cluster address).
 __device__ __forceinline__ void tma_load_2d_pair(void* dst, const void* desc, uint32_t bar_cluster_addr, int32_t x,
