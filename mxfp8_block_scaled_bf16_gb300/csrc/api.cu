@@ -32,11 +32,13 @@ struct DeviceInit {
 // The CTA-pair GEMM kernel is used only when NVQ_GEMM_PAIR=1 is set in the
 // environment: it is exact, but on the Llama-3-8B shapes its MMA stream runs
 // slower than the single-CTA kernel's.
+// The CTA-pair kernel runs the GEMMs whose output width is a multiple of 256
+// unless NVQ_GEMM_PAIR=0 (the single-CTA kernel then takes them too).
 bool pair_gemm_enabled()
 {
     static const bool on = [] {
         const char* e = std::getenv("NVQ_GEMM_PAIR");
-        return e && e[0] == '1';
+        return !(e && e[0] == '0');
     }();
     return on;
 }
@@ -307,6 +309,21 @@ nvq_status gemm_prepare(const nvq_qtensor* A, const nvq_qtensor* B, int64_t n_ou
     return s;
 }
 
+// bf16 C viewed as [rows][ncols] with row pitch ldc, stored in boxes of 32
+// rows x 64 columns (128 bytes, 128B swizzle) by the CTA-pair epilogue.
+nvq_status make_c_map(CUtensorMap* map, void* C, int64_t rows, int64_t ncols, int64_t ldc)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return NVQ_ERR_CUDA;
+    cuuint64_t dims[2] = {(cuuint64_t)ncols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)(ldc * 2)};
+    cuuint32_t box[2] = {64, 32};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, C, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? NVQ_OK : NVQ_ERR_CUDA;
+}
+
 nvq_status check_c(const void* C, int64_t ldc, int64_t ncols, int c_fp32)
 {
     if (!C) return NVQ_ERR_NULL;
@@ -316,7 +333,7 @@ nvq_status check_c(const void* C, int64_t ldc, int64_t ncols, int c_fp32)
     return NVQ_OK;
 }
 
-nvq_status gemm_launch(const CUtensorMap& am, const CUtensorMap& bm, GemmArgs& g, cudaStream_t stream)
+nvq_status gemm_launch(const CUtensorMap& am, const CUtensorMap& bm, GemmArgs& g, int64_t n_out, cudaStream_t stream)
 {
     int* status = nullptr;
     int num_sms = 0;
@@ -334,7 +351,20 @@ nvq_status gemm_launch(const CUtensorMap& am, const CUtensorMap& bm, GemmArgs& g
     bool st32 = !g.c_fp32 && (reinterpret_cast<uintptr_t>(g.C) & 31) == 0 && g.ldc % 16 == 0;
     for (int i = 0; i < g.G && st32; ++i) st32 = g.groups[i].c_off % 16 == 0;
     g.c_st32 = st32 ? 1 : 0;
-    if (g.use_pair) return cuda_status(launch_gemm_pair(&am, &bm, g, num_sms, stream));
+    // C rows written by this call, and the C row of each group's first row
+    int64_t rows_end = 0;
+    for (int i = 0; i < g.G; ++i) {
+        const int64_t r0 = g.ldc > 0 ? g.groups[i].c_off / g.ldc : 0;
+        g.groups[i].c_row0 = (int32_t)r0;
+        if (g.groups[i].rows_valid > 0 && r0 + g.groups[i].rows_valid > rows_end) rows_end = r0 + g.groups[i].rows_valid;
+    }
+    CUtensorMap cm;
+    std::memset(&cm, 0, sizeof cm);
+    g.c_tma = 0;
+    if (g.use_pair && !g.c_fp32 && rows_end > 0 && rows_end <= INT32_MAX &&
+        make_c_map(&cm, g.C, rows_end, n_out, g.ldc) == NVQ_OK)
+        g.c_tma = 1;
+    if (g.use_pair) return cuda_status(launch_gemm_pair(&am, &bm, &cm, g, num_sms, stream));
     return cuda_status(launch_gemm(&am, &bm, g, num_sms, stream));
 }
 
@@ -445,7 +475,7 @@ nvq_status nvq_gemm_tn(const nvq_qtensor* A, const nvq_qtensor* B, const void* b
         gr.m_tiles = g->total_m_tiles;
         gr.k_len = (int32_t)A->cols;
         gr.rows_valid = (int32_t)A->rows;
-        s = gemm_launch(am, bm, *g, reinterpret_cast<cudaStream_t>(stream));
+        s = gemm_launch(am, bm, *g, B->rows, reinterpret_cast<cudaStream_t>(stream));
     }
     delete g;
     return s;
@@ -565,7 +595,7 @@ nvq_status nvq_grouped_gemm_rows(const nvq_qtensor* A, const nvq_qtensor* B, con
             orow += group_rows[i];
         }
         g->total_m_tiles = (int)tiles;
-        s = gemm_launch(am, bm, *g, reinterpret_cast<cudaStream_t>(stream));
+        s = gemm_launch(am, bm, *g, n_out, reinterpret_cast<cudaStream_t>(stream));
     }
     delete g;
     return s;
@@ -609,7 +639,7 @@ nvq_status nvq_grouped_gemm_wgrad(const nvq_qtensor* A, const nvq_qtensor* B, co
             pk += kl;
         }
         g->total_m_tiles = (int)(G * mt);
-        s = gemm_launch(am, bm, *g, reinterpret_cast<cudaStream_t>(stream));
+        s = gemm_launch(am, bm, *g, B->rows, reinterpret_cast<cudaStream_t>(stream));
     }
     delete g;
     return s;

@@ -12,10 +12,10 @@
 // (128 rows x 256 fp32 columns).  Per CTA a stage holds 32 KB of operands
 // (against 48 KB for a 128x256 tile in one CTA) plus the A scales of its rows
 // and the B scales of all 256 columns (the pair MMA reads the full B scale
-// set from each CTA's TMEM), so five stages fit (NVFP4) and each SM moves
-// less data from L2 per MMA FLOP.  On the Llama-3-8B shapes the pair MMA
-// stream itself ran slower than the single-CTA one, so this kernel is only
-// used when NVQ_GEMM_PAIR=1 is set; it is kept exact and tested.
+// set from each CTA's TMEM), so each SM writes less into shared memory per
+// MMA FLOP.  bf16 outputs leave through 4 KB per-warp staging buffers and
+// TMA tensor stores (full 128-byte lines).  This kernel takes every GEMM whose
+// output width is a multiple of 256 unless NVQ_GEMM_PAIR=0.
 //
 // Signalling (every wait bounded, as in gemm.cu):
 //   full[s]      leader: A/B bytes of both CTAs (each CTA's TMA load signals the
@@ -64,7 +64,8 @@ struct Cfg {
     static constexpr int kSfaBytes = kAtomsK * 512;
     static constexpr int kSfbBytes = kAtomsK * 512 * kSfbHalves;
     static constexpr int kStageBytes = 2 * kHalfTileBytes + kSfaBytes + kSfbBytes;
-    static constexpr int kStagesFit = (232448 - 1024 - 512) / kStageBytes;
+    static constexpr int kEpiBytes = kEpiWarps * 4096;  // TMA-store staging, 4 KB per epilogue warp
+    static constexpr int kStagesFit = (232448 - 1024 - 1024 - kEpiBytes) / kStageBytes;
     static constexpr int kStages = kStagesFit < 6 ? kStagesFit : 6;
     static constexpr uint32_t kSfaCols = 4 * kAtomsK;
     static constexpr uint32_t kSfbCols = 4 * kAtomsK * kSfbHalves;
@@ -78,7 +79,8 @@ struct Cfg {
     static constexpr int kBar = kSfb + kStages * kSfbBytes;
     static constexpr int kNumBars = 4 * kStages + 3;  // full, empty, sf_full, sf_ready, acc_full, acc_empty, done
     static constexpr int kMisc = kBar + kNumBars * 8;
-    static constexpr int kAlloc = kMisc + 16 + 1024;
+    static constexpr int kEpi = (kMisc + 16 + 1023) / 1024 * 1024;
+    static constexpr int kAlloc = kEpi + kEpiBytes + 1024;
     static_assert(kAlloc <= 232448, "shared memory budget");
 };
 
@@ -158,7 +160,7 @@ __device__ __forceinline__ void arrive_leader(uint64_t* bar, uint32_t rank)
 template <int FMT, bool SFB_FULL>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap a_map, const __grid_constant__ CUtensorMap b_map,
-                     const __grid_constant__ GemmArgs args)
+                     const __grid_constant__ CUtensorMap c_map, const __grid_constant__ GemmArgs args)
 {
     using C = Cfg<FMT, SFB_FULL>;
     extern __shared__ uint8_t smem_raw[];
@@ -378,12 +380,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const int col0 = tl.n_tile * BN + half * kCols;
             const int64_t rowoff = gr.c_off + (int64_t)out_row * args.ldc + col0;
             const uint32_t taddr = tmem_base + (uint32_t)(half * kCols) + ((uint32_t)(quad * 32) << 16);
-            epilogue_slice<kCols>(args, taddr, tl.num_kb > 0, alpha, col0, rowoff, row_ok, [&] {
+            auto release = [&] {
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) arrive_leader(acc_empty, rank);
-            });
+            };
+            if (args.c_tma && tl.mt_local * BM + BM <= gr.rows_valid)
+                epilogue_slice_tma<kCols>(args, &c_map, smem + C::kEpi + (warp - kFirstEpiWarp) * 4096, taddr,
+                                          tl.num_kb > 0, alpha, col0, gr.c_row0 + tl.mt_local * BM + quad * 32, lane,
+                                          release);
+            else
+                epilogue_slice<kCols>(args, taddr, tl.num_kb > 0, alpha, col0, rowoff, row_ok, release);
         }
+        if (lane == 0) bulk_wait_group0();  // this warp's C stores completed before the CTA exits
     }
 
     tc_fence_before();
@@ -412,20 +421,22 @@ cudaError_t init_gemm_pair_attributes()
     return e;
 }
 
-cudaError_t launch_gemm_pair(const void* a_map, const void* b_map, const GemmArgs& g, int num_sms, cudaStream_t s)
+cudaError_t launch_gemm_pair(const void* a_map, const void* b_map, const void* c_map, const GemmArgs& g, int num_sms,
+                             cudaStream_t s)
 {
     const int tiles = g.total_pm_tiles * g.n_tiles;
     if (tiles == 0) return cudaSuccess;
     const int pairs = tiles < num_sms / 2 ? tiles : num_sms / 2;
     const CUtensorMap& am = *reinterpret_cast<const CUtensorMap*>(a_map);
     const CUtensorMap& bm = *reinterpret_cast<const CUtensorMap*>(b_map);
+    const CUtensorMap& cm = *reinterpret_cast<const CUtensorMap*>(c_map);
     constexpr bool kFull = NVQ_PAIR_SFB_FULL != 0;
     if (g.fmt == 1)
         gemm2::gemm_pair_kernel<1, kFull>
-            <<<2 * pairs, gemm2::kThreads, gemm2::Cfg<1, kFull>::kAlloc, s>>>(am, bm, g);
+            <<<2 * pairs, gemm2::kThreads, gemm2::Cfg<1, kFull>::kAlloc, s>>>(am, bm, cm, g);
     else
         gemm2::gemm_pair_kernel<2, kFull>
-            <<<2 * pairs, gemm2::kThreads, gemm2::Cfg<2, kFull>::kAlloc, s>>>(am, bm, g);
+            <<<2 * pairs, gemm2::kThreads, gemm2::Cfg<2, kFull>::kAlloc, s>>>(am, bm, cm, g);
     return cudaGetLastError();
 }
 

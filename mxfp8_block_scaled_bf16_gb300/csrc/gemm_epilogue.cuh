@@ -3,47 +3,58 @@
 // kCols fp32 columns) into C = alpha * acc (+ bias) rows.
 #pragma once
 
+#include <cuda.h>
+
 #include "nvq_device.cuh"
 #include "nvq_kernels.h"
 
 namespace nvq {
 
-// taddr: TMEM address of the warp's slice (its lane quadrant, first column);
-// have_k: false for an empty contraction (the slice is zero); rowoff: element
-// offset of the row's first column in C; release(): hands the accumulator
-// back to the MMA issuer once every TMEM load of the slice has completed.
+// Reads the warp's slice in 32-column chunks, scales, adds the bias and packs
+// to bf16 pairs (column 2i in the low half of packed[i]).  taddr: TMEM address
+// of the slice (its lane quadrant, first column); have_k: false for an empty
+// contraction (the slice is zero).
+template <int kCols>
+__device__ __forceinline__ void pack_slice_bf16(const GemmArgs& args, uint32_t taddr, bool have_k, float alpha,
+                                                int col0, uint32_t (&packed)[kCols / 2])
+{
+#pragma unroll
+    for (int c = 0; c < kCols / 32; ++c) {
+        uint32_t v[32];
+        if (have_k) {
+            tmem_ld_32x32b_x32(taddr + (uint32_t)(c * 32), v);
+            tmem_ld_wait();
+        } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = 0u;
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            float y0 = __fmul_rn(alpha, __uint_as_float(v[2 * i]));
+            float y1 = __fmul_rn(alpha, __uint_as_float(v[2 * i + 1]));
+            if (args.bias) {
+                y0 = __fadd_rn(y0, __uint_as_float((uint32_t)args.bias[col0 + c * 32 + 2 * i] << 16));
+                y1 = __fadd_rn(y1, __uint_as_float((uint32_t)args.bias[col0 + c * 32 + 2 * i + 1] << 16));
+            }
+            __nv_bfloat162 b2 = __floats2bfloat162_rn(y0, y1);
+            packed[c * 16 + i] = *reinterpret_cast<uint32_t*>(&b2);
+        }
+    }
+}
+
+// rowoff: element offset of the row's first column in C; release(): hands the
+// accumulator back to the MMA issuer once every TMEM load of the slice has
+// completed.
 template <int kCols, typename Release>
 __device__ __forceinline__ void epilogue_slice(const GemmArgs& args, uint32_t taddr, bool have_k, float alpha,
                                                int col0, int64_t rowoff, bool row_ok, Release release)
 {
     static_assert(kCols % 64 == 0, "64-column granularity");
     if (!args.c_fp32) {
-        // bf16: read the whole slice in 32-column chunks, scale, add the bias
-        // and pack in registers, release the accumulator, then store -- the
-        // next tile's MMAs overlap the global stores.
+        // bf16: pack the whole slice in registers, release the accumulator,
+        // then store -- the next tile's MMAs overlap the global stores.
         uint32_t packed[kCols / 2];
-#pragma unroll
-        for (int c = 0; c < kCols / 32; ++c) {
-            uint32_t v[32];
-            if (have_k) {
-                tmem_ld_32x32b_x32(taddr + (uint32_t)(c * 32), v);
-                tmem_ld_wait();
-            } else {
-#pragma unroll
-                for (int i = 0; i < 32; ++i) v[i] = 0u;
-            }
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                float y0 = __fmul_rn(alpha, __uint_as_float(v[2 * i]));
-                float y1 = __fmul_rn(alpha, __uint_as_float(v[2 * i + 1]));
-                if (args.bias) {
-                    y0 = __fadd_rn(y0, __uint_as_float((uint32_t)args.bias[col0 + c * 32 + 2 * i] << 16));
-                    y1 = __fadd_rn(y1, __uint_as_float((uint32_t)args.bias[col0 + c * 32 + 2 * i + 1] << 16));
-                }
-                __nv_bfloat162 b2 = __floats2bfloat162_rn(y0, y1);
-                packed[c * 16 + i] = *reinterpret_cast<uint32_t*>(&b2);
-            }
-        }
+        pack_slice_bf16<kCols>(args, taddr, have_k, alpha, col0, packed);
         release();
         if (!row_ok) return;
         if (args.c_st32) {  // 32-byte stores, one full L2 sector each
@@ -83,6 +94,42 @@ __device__ __forceinline__ void epilogue_slice(const GemmArgs& args, uint32_t ta
                 f[e] = y;
             }
             dst[i] = make_float4(f[0], f[1], f[2], f[3]);
+        }
+    }
+}
+
+// bf16 slice whose 32 rows are all valid, stored through the TMA: the warp
+// writes 32 rows x 64 columns (4 KB, 128-byte rows, 128B-swizzled as the
+// store's tensor map expects) into its staging buffer, and one lane issues a
+// bulk tensor store, so every global write is a full 128-byte line (register
+// stores write one 32-byte sector per row and instruction, and their L1
+// traffic slowed the tensor pipe).  stage: 1024-byte aligned, 4 KB, owned by
+// this warp; c_row0: C row of the slice's first row.  The lane that issues the
+// stores waits for their completion before the CTA exits.
+template <int kCols, typename Release>
+__device__ __forceinline__ void epilogue_slice_tma(const GemmArgs& args, const CUtensorMap* c_map, uint8_t* stage,
+                                                   uint32_t taddr, bool have_k, float alpha, int col0, int c_row0,
+                                                   int lane, Release release)
+{
+    static_assert(kCols % 64 == 0, "64-column granularity");
+    uint32_t packed[kCols / 2];
+    pack_slice_bf16<kCols>(args, taddr, have_k, alpha, col0, packed);
+    release();
+    uint8_t* row = stage + lane * 128;
+#pragma unroll
+    for (int b = 0; b < kCols / 64; ++b) {
+        if (lane == 0) bulk_wait_group_read0();  // the previous store has read the buffer
+        __syncwarp();
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<uint4*>(row + ((c ^ (lane & 7)) << 4)) =
+                make_uint4(packed[32 * b + 4 * c], packed[32 * b + 4 * c + 1], packed[32 * b + 4 * c + 2],
+                           packed[32 * b + 4 * c + 3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            tma_store_2d(c_map, stage, col0 + 64 * b, c_row0);
+            bulk_commit_group();
         }
     }
 }

@@ -66,6 +66,7 @@ struct GemmGroup {
     int32_t rows_valid; // output rows written (<= m_tiles * 128)
     int32_t amax_idx;   // index into the amax arrays (NVFP4 alpha)
     int64_t c_off;      // element offset of the group's C[0][0]
+    int32_t c_row0;     // C row of the group's first row (c_off / ldc)
 };
 
 struct GemmArgs {
@@ -88,6 +89,7 @@ struct GemmArgs {
     int64_t ldc;
     int c_fp32;
     int c_st32;  // bf16 C, base and row pitch 32-byte aligned: 32-byte stores
+    int c_tma;   // bf16 C stored through the C tensor map (CTA-pair kernel)
     int* status;           // device status word
     int debug_drop_first_load;  // test hook: arm stage 0's barrier but issue no copy
     GemmGroup groups[kMaxGroups];
@@ -103,7 +105,8 @@ cudaError_t launch_gemm(const void* a_map, const void* b_map, const GemmArgs& g,
 cudaError_t init_gemm_attributes();
 
 // CTA-pair (cta_group::2) kernel for block_n == 256: 2 * min(tiles, num_sms / 2) CTAs.
-cudaError_t launch_gemm_pair(const void* a_map, const void* b_map, const GemmArgs& g, int num_sms, cudaStream_t s);
+cudaError_t launch_gemm_pair(const void* a_map, const void* b_map, const void* c_map, const GemmArgs& g, int num_sms,
+                             cudaStream_t s);
 cudaError_t init_gemm_pair_attributes();
 
 }  // namespace nvq
