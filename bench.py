@@ -39,12 +39,12 @@ CONFIG = {"workload": "llama3_8b_mlp_up_fwd_dgrad_wgrad", "M_tokens": M, "N_out"
 # fp4 dense / bf16 dense nominal ratio (13.5 / 2.25 PFLOP/s) applied to the measured bf16 peak
 FP4_OVER_BF16 = 6.0
 # dram__bytes_read.sum + dram__bytes_write.sum per launch from ncu captures of the
-# current kernels on this workload (profiles/gemm_nvfp4_bn256_llama3_8b_fwd.md: the
+# current kernels on this workload (profiles/gemm_pair_nvfp4_llama3_8b_fwd.md: the
 # forward GEMM launch; profiles/quantize_nvfp4_llama3_8b.md: the six amax + quantize
 # launches of one step).  Set to None whenever those kernels change.
-GEMM_TRAFFIC_BYTES = (87.320832 + 421.958912) * 1e6
+GEMM_TRAFFIC_BYTES = (105.819904 + 429.165312) * 1e6
 QUANT_TRAFFIC_BYTES = (134.253 + 3.287 + 117.472 + 3.250 + 469.814 + 3.213
-                       + 134.319 + 42.950 + 117.512 + 34.815 + 469.965 + 232.159) * 1e6
+                       + 134.319 + 42.950 + 117.512 + 34.815 + 469.963 + 231.960) * 1e6
 
 
 def _env_int(name, default):
@@ -320,7 +320,7 @@ def run_ours(args, rank, world, local_rank):
         "vs_baseline": None, "dtype": "nvfp4", "data": "synthetic", "config": CONFIG,
         "gpu_launches": 9 * args.steps,
         "launch_mode": "eager" if args.eager else "cuda_graph",
-        "roofline": {"bound": "tensor", "kernel": "gemm_kernel<NVFP4> (fwd, dgrad, wgrad)",
+        "roofline": {"bound": "tensor", "kernel": "gemm_pair_kernel<NVFP4> (CTA pair; fwd, dgrad, wgrad)",
                      "achieved": achieved, "peak": peak_fp4, "unit": "TFLOP/s", "frac": achieved / peak_fp4,
                      "traffic": GEMM_TRAFFIC_BYTES, "traffic_note": "bytes per launch, ncu capture of the forward GEMM",
                      "peak_note": f"{src} bf16 sustained x {FP4_OVER_BF16} (fp4/bf16 nominal dense ratio)"},
