@@ -570,8 +570,42 @@ def run_moe_grouped(args, nvq, inputs):
 
     ms = _graph_ms(step, args.steps, args.warmup, args.eager)
     flop = 3 * 2.0 * T * Nn * Kk
+
+    # per-phase times from an eager pass with events between the calls
+    names = ["quant_x", "quant_w", "gemm_fwd_nvfp4", "quant_dy", "gemm_dgrad_mxfp8", "gemm_wgrad_mxfp8"]
+    calls = [lambda: nvq.grouped_hybrid_quantize(x, sizes, nvq.NVFP4, nvq.MXFP8, out_row=xr, out_col=xc),
+             lambda: nvq.grouped_hybrid_quantize(w2, [Nn] * G, nvq.NVFP4, nvq.MXFP8, out_row=wr, out_col=wc),
+             lambda: nvq.grouped_gemm_rows(xr, wr, sizes, Nn, b_col_groups=False, out=y),
+             lambda: nvq.grouped_hybrid_quantize(dy, sizes, nvq.MXFP8, nvq.MXFP8, out_row=dr, out_col=dc),
+             lambda: nvq.grouped_gemm_rows(dr, wc, sizes, Nn, b_col_groups=True, out=dx),
+             lambda: nvq.grouped_gemm_wgrad(dc, xc, sizes, out=dwt)]
+    acc = [0.0] * len(calls)
+    reps = 5
+    for _ in range(reps):
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)]
+        ev[0].record()
+        for i, c in enumerate(calls):
+            c()
+            ev[i + 1].record()
+        torch.cuda.synchronize()
+        for i in range(len(calls)):
+            acc[i] += ev[i].elapsed_time(ev[i + 1]) / reps
+    breakdown = dict(zip(names, acc))
+    peaks, _src = _peaks()
+    gemm_flop = 2.0 * T * Nn * Kk
+    fp4_peak = peaks["bf16_tflops_sustained"] * FP4_OVER_BF16
+    fp8_peak = peaks["bf16_tflops_sustained"] * 2.0
+    rates = {"gemm_fwd_nvfp4": gemm_flop / (acc[2] * 1e-3) / 1e12, "gemm_dgrad_mxfp8": gemm_flop / (acc[4] * 1e-3) / 1e12,
+             "gemm_wgrad_mxfp8": gemm_flop / (acc[5] * 1e-3) / 1e12}
     return {"metric": "MoE grouped hybrid linear fwd+dgrad+wgrad TFLOP/s (64 experts 4096->1536)",
             "value": flop / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms,
+            "breakdown_ms_eager": breakdown,
+            "gemm_tflops": rates,
+            "gemm_frac": {"gemm_fwd_nvfp4": rates["gemm_fwd_nvfp4"] / fp4_peak,
+                          "gemm_dgrad_mxfp8": rates["gemm_dgrad_mxfp8"] / fp8_peak,
+                          "gemm_wgrad_mxfp8": rates["gemm_wgrad_mxfp8"] / fp8_peak},
+            "peak_note": "FP4 = measured bf16 sustained x 6, FP8 = x 2 (nominal dense ratios); GEMM FLOPs count "
+                         "unpadded tokens",
             "dtype": "nvfp4 fwd / mxfp8 bwd",
             "config": {"workload": "moe_grouped_64x4096x1536_zipf1.1", "tokens": T, "experts": G,
                        "group_sizes_min_max": [min(sizes), max(sizes)], "padded_rows": P},

@@ -334,6 +334,13 @@ __global__ void __launch_bounds__(kThreads, 2) quantize_kernel(QuantArgs a)
         }
     }
 
+    // The rowwise pass is done with t: pin its registers here so the compiler
+    // does not start the columnwise extraction inside the rowwise pass (that
+    // overlap spilled registers in the variants without the Hadamard transform).
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+        asm volatile("" : "+r"(t.w[i].x), "+r"(t.w[i].y), "+r"(t.w[i].z), "+r"(t.w[i].w));
+
     // ---------------- columnwise direction (output row = column k, contraction = padded row p)
     if constexpr (COL_FMT == 1) {  // NVFP4: the thread's 16 rows form one block per column
         const Nvfp4Scale ts = nvfp4_tensor_scale(a.col_amax[g]);
