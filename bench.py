@@ -43,8 +43,8 @@ FP4_OVER_BF16 = 6.0
 # forward GEMM launch; profiles/quantize_nvfp4_llama3_8b.md: the six amax + quantize
 # launches of one step).  Set to None whenever those kernels change.
 GEMM_TRAFFIC_BYTES = (105.819904 + 429.165312) * 1e6
-QUANT_TRAFFIC_BYTES = (134.253 + 3.287 + 117.472 + 3.250 + 469.814 + 3.213
-                       + 134.319 + 42.950 + 117.512 + 34.815 + 469.963 + 231.960) * 1e6
+QUANT_TRAFFIC_BYTES = (134.246 + 2.945 + 134.292 + 39.713 + 117.470 + 0.058
+                       + 117.508 + 29.497 + 469.891 + 0.200 + 469.986 + 228.763) * 1e6
 
 
 def _env_int(name, default):

@@ -97,6 +97,23 @@ __device__ __forceinline__ void flip_rows(ThreadTile& t, uint32_t sign_mask)
     }
 }
 
+// H16 u for an already sign-flipped u: butterflies with spans 1, 2, 4, 8
+// ((a, b) -> (a + b, a - b)), without the 1/4.
+__device__ __forceinline__ void butterfly16(float (&u)[16])
+{
+#pragma unroll
+    for (int h = 1; h < 16; h <<= 1) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            if ((i & h) == 0) {
+                const float a = u[i], b = u[i + h];
+                u[i] = __fadd_rn(a, b);
+                u[i + h] = __fsub_rn(a, b);
+            }
+        }
+    }
+}
+
 // T(u) = 1/4 H16 u for an already sign-flipped u: butterflies with spans
 // 1, 2, 4, 8 ((a, b) -> (a + b, a - b)), then the exact 1/4.
 __device__ __forceinline__ void hadamard16(float (&u)[16])
@@ -154,10 +171,13 @@ __global__ void __launch_bounds__(kThreads, 2) amax_kernel(QuantArgs a)
         for (int j = 0; j < 8; ++j) {
             float u[16];
             column16(t, j, u);
-            hadamard16(u);
+            butterfly16(u);
 #pragma unroll
             for (int i = 0; i < 16; ++i) m_rht = fmaxf(m_rht, fabsf(u[i]));
         }
+        // max |fl(u/4)| = fl(max |u| / 4): rounding is monotonic, so the 1/4 of
+        // the transform is applied once to the maximum
+        m_rht = __fmul_rn(m_rht, 0.25f);
     }
     __shared__ float red[2][kThreads / 32];
     m_plain = warp_max(m_plain);
