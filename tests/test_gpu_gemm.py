@@ -183,3 +183,26 @@ def test_linear_fwd_dgrad_wgrad(M, N, K):
     xf = (bits(x).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
     rel = np.linalg.norm(dw.float().cpu().numpy() - dyf.T @ xf) / np.linalg.norm(dyf.T @ xf)
     assert rel < 0.25
+
+
+@pytest.mark.parametrize("col_off", [128, 8])
+def test_strided_output_matches_contiguous(col_off):
+    """C written into a column slice of a wider tensor (ldc > N, base offset
+    col_off elements: 256 B or 16 B) equals the contiguous result bit for bit,
+    and nothing outside the slice is touched (both output paths: the CTA-pair
+    kernel's TMA tensor stores and, under NVQ_GEMM_PAIR=0, the single-CTA
+    kernel's 32-byte or 16-byte register stores)."""
+    M, N, K = 384, 512, 512
+    x = _randn(M, K, seed=21)
+    w = _randn(N, K, seed=22, std=0.05)
+    xr, _ = nvq.nvfp4_quantize(x.cuda(), nvq.DIR_ROW)
+    wr, _ = nvq.nvfp4_quantize(w.cuda(), nvq.DIR_ROW)
+    ref = nvq.gemm_tn(xr, wr)
+    big = torch.full((M, N + 384), 7.0, dtype=torch.bfloat16, device="cuda")
+    view = big[:, col_off:col_off + N]
+    nvq.gemm_tn(xr, wr, out=view)
+    torch.cuda.synchronize()
+    assert view.stride(0) == N + 384
+    assert torch.equal(view, ref)
+    outside = torch.cat([big[:, :col_off], big[:, col_off + N:]], dim=1)
+    assert torch.all(outside == 7.0)
