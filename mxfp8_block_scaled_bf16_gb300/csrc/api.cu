@@ -29,9 +29,6 @@ struct DeviceInit {
     cudaError_t err = cudaSuccess;
 };
 
-// The CTA-pair GEMM kernel is used only when NVQ_GEMM_PAIR=1 is set in the
-// environment: it is exact, but on the Llama-3-8B shapes its MMA stream runs
-// slower than the single-CTA kernel's.
 // The CTA-pair kernel runs the GEMMs whose output width is a multiple of 256
 // unless NVQ_GEMM_PAIR=0 (the single-CTA kernel then takes them too).
 bool pair_gemm_enabled()

@@ -47,20 +47,16 @@ constexpr int kScaleLoadWarp = kFirstEpiWarp + kEpiWarps;  // block-scale copies
 constexpr int kThreads = 32 * (kScaleLoadWarp + 1);
 constexpr uint32_t kTmemCols = 512;
 
-// SFB_FULL: each CTA's TMEM holds the B scales of all 256 columns (both
-// halves) -- the layout the pair MMA reads; holding only the scales of the B
-// half a CTA stages gives wrong products.
-#ifndef NVQ_PAIR_SFB_FULL
-#define NVQ_PAIR_SFB_FULL 1
-#endif
-
-template <int FMT, bool SFB_FULL>
+// Each CTA's TMEM holds the B scales of all 256 columns (both halves of B):
+// the pair MMA reads the full B scale set from each CTA's TMEM (holding only
+// the half a CTA stages gives wrong products).
+template <int FMT>
 struct Cfg {
     static constexpr int kStageK = FMT == 1 ? 256 : 128;
     static constexpr int kMmaK = FMT == 1 ? 64 : 32;
     static constexpr int kAtomsK = FMT == 1 ? 4 : 1;
     static constexpr int kElemPerAtom = FMT == 1 ? 64 : 128;
-    static constexpr int kSfbHalves = SFB_FULL ? 2 : 1;
+    static constexpr int kSfbHalves = 2;
     static constexpr int kSfaBytes = kAtomsK * 512;
     static constexpr int kSfbBytes = kAtomsK * 512 * kSfbHalves;
     static constexpr int kStageBytes = 2 * kHalfTileBytes + kSfaBytes + kSfbBytes;
@@ -157,12 +153,12 @@ __device__ __forceinline__ void arrive_leader(uint64_t* bar, uint32_t rank)
     else mbar_arrive_cluster_relaxed(map_to_rank(bar, 0));
 }
 
-template <int FMT, bool SFB_FULL>
+template <int FMT>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap a_map, const __grid_constant__ CUtensorMap b_map,
                      const __grid_constant__ CUtensorMap c_map, const __grid_constant__ GemmArgs args)
 {
-    using C = Cfg<FMT, SFB_FULL>;
+    using C = Cfg<FMT>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kBar);
@@ -335,13 +331,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     const uint32_t sf_bytes = (uint32_t)atoms * 512u;
                     mbar_arrive_expect_tx_if(&sf_full[s], sf_bytes * (1 + C::kSfbHalves), live);
                     n_armed += live;
-                    const int b_row = tl.b_row_pair + (int)rank * 128;
                     bulk_load_if(smem + C::kSfa + s * C::kSfaBytes,
                                  args.a_scale + ((int64_t)(tl.a_row / 128) * args.a_scale_ctiles + ka / C::kElemPerAtom) * 512,
                                  sf_bytes, &sf_full[s], live);
 #pragma unroll
                     for (int h = 0; h < C::kSfbHalves; ++h) {
-                        const int brow = SFB_FULL ? tl.b_row_pair + h * 128 : b_row;
+                        const int brow = tl.b_row_pair + h * 128;
                         bulk_load_if(smem + C::kSfb + s * C::kSfbBytes + h * C::kAtomsK * 512,
                                      args.b_scale + ((int64_t)(brow / 128) * args.b_scale_ctiles + kbb / C::kElemPerAtom) * 512,
                                      sf_bytes, &sf_full[s], live);
@@ -407,8 +402,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 template <int FMT>
 cudaError_t set_smem()
 {
-    using C = Cfg<FMT, NVQ_PAIR_SFB_FULL != 0>;
-    return cudaFuncSetAttribute(gemm_pair_kernel<FMT, NVQ_PAIR_SFB_FULL != 0>,
+    using C = Cfg<FMT>;
+    return cudaFuncSetAttribute(gemm_pair_kernel<FMT>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, C::kAlloc);
 }
 
@@ -430,13 +425,10 @@ cudaError_t launch_gemm_pair(const void* a_map, const void* b_map, const void* c
     const CUtensorMap& am = *reinterpret_cast<const CUtensorMap*>(a_map);
     const CUtensorMap& bm = *reinterpret_cast<const CUtensorMap*>(b_map);
     const CUtensorMap& cm = *reinterpret_cast<const CUtensorMap*>(c_map);
-    constexpr bool kFull = NVQ_PAIR_SFB_FULL != 0;
     if (g.fmt == 1)
-        gemm2::gemm_pair_kernel<1, kFull>
-            <<<2 * pairs, gemm2::kThreads, gemm2::Cfg<1, kFull>::kAlloc, s>>>(am, bm, cm, g);
+        gemm2::gemm_pair_kernel<1><<<2 * pairs, gemm2::kThreads, gemm2::Cfg<1>::kAlloc, s>>>(am, bm, cm, g);
     else
-        gemm2::gemm_pair_kernel<2, kFull>
-            <<<2 * pairs, gemm2::kThreads, gemm2::Cfg<2, kFull>::kAlloc, s>>>(am, bm, cm, g);
+        gemm2::gemm_pair_kernel<2><<<2 * pairs, gemm2::kThreads, gemm2::Cfg<2>::kAlloc, s>>>(am, bm, cm, g);
     return cudaGetLastError();
 }
 
