@@ -43,8 +43,7 @@ FP4_OVER_BF16 = 6.0
 # forward GEMM launch; profiles/quantize_nvfp4_llama3_8b.md: the six amax + quantize
 # launches of one step).  Set to None whenever those kernels change.
 GEMM_TRAFFIC_BYTES = (105.819904 + 429.165312) * 1e6
-QUANT_TRAFFIC_BYTES = (134.246 + 2.945 + 134.292 + 39.713 + 117.470 + 0.058
-                       + 117.508 + 29.497 + 469.891 + 0.200 + 469.986 + 228.763) * 1e6
+QUANT_TRAFFIC_BYTES = None  # the quantize kernels changed since the last capture
 
 
 def _env_int(name, default):

@@ -218,17 +218,56 @@ __device__ __forceinline__ Nvfp4Scale nvfp4_tensor_scale(float A)
     return s;
 }
 
-// Block scale code and element encode factor for block amax b.
-__device__ __forceinline__ uint32_t nvfp4_block_scale(const Nvfp4Scale& ts, float b, float& e)
+// Block scale code S and element encode factor e = fl(s_enc / E4M3(S)) for
+// block amax b, without a division per block: every finite E4M3 value is
+// n * 2^j with n in 1..15 (normal codes: n = 8 + mantissa, j = exponent - 10;
+// subnormal codes: n = mantissa, j = -9), so e = fl(s_enc / n) * 2^-j.  The
+// power-of-two scaling is exact because s_enc / n and e stay normal for every
+// finite tensor amax (e >= (2688 / FLT_MAX) / 448 > FLT_MIN), and it
+// overflows exactly when the quotient does.  q_tab[n] = fl(s_enc / n).
+__device__ __forceinline__ uint32_t nvfp4_block_scale(const Nvfp4Scale& ts, const float* q_tab, float b, float& e)
 {
     uint32_t S = 0;
     if (b != 0.0f && !ts.zero) S = e4m3_rn(__fmul_rn(b, ts.r448));
     e = 0.0f;
     if (S != 0) {
-        float q = __fdiv_rn(ts.s_enc, e4m3_to_f32(S));
+        const uint32_t ex = S >> 3, mant = S & 7u;
+        const uint32_t n = ex ? 8u + mant : mant;
+        const uint32_t ex1 = ex ? ex : 1u;
+        const float q = __fmul_rn(q_tab[n], __uint_as_float((137u - ex1) << 23));  // * 2^(10 - ex1)
         e = isinf(q) ? 3.402823466e38f : q;
     }
     return S;
+}
+
+// The same by division (kept for the NVFP4-row + MXFP8-column variant, where
+// the table version made the compiler spill registers).
+__device__ __forceinline__ uint32_t nvfp4_block_scale_div(const Nvfp4Scale& ts, float b, float& e)
+{
+    uint32_t S = 0;
+    if (b != 0.0f && !ts.zero) S = e4m3_rn(__fmul_rn(b, ts.r448));
+    e = 0.0f;
+    if (S != 0) {
+        const float q = __fdiv_rn(ts.s_enc, e4m3_to_f32(S));
+        e = isinf(q) ? 3.402823466e38f : q;
+    }
+    return S;
+}
+
+// q_tab[dir][n] = fl(s_enc / n), n = 1..15, of the row (dir 0) and column
+// (dir 1) NVFP4 tensor scales of group g; threads 0..31 fill it, the caller
+// synchronizes before use.
+template <int ROW_FMT, int COL_FMT>
+__device__ __noinline__ void nvfp4_fill_q_tab(const QuantArgs& a, int g, float (&q_tab)[2][16])
+{
+    if (threadIdx.x < 32) {
+        const int dir = threadIdx.x >> 4, n = threadIdx.x & 15;
+        float A = 0.0f;
+        if (dir == 0 && ROW_FMT == 1) A = a.row_amax[g];
+        if (dir == 1 && COL_FMT == 1) A = a.col_amax[g];
+        const Nvfp4Scale ts = nvfp4_tensor_scale(A);
+        q_tab[dir][n] = n ? __fdiv_rn(ts.s_enc, (float)n) : 0.0f;
+    }
 }
 
 // 8 consecutive elements of one direction's output starting at linear index L0
@@ -303,9 +342,13 @@ __global__ void __launch_bounds__(kThreads, 2) quantize_kernel(QuantArgs a)
         reinterpret_cast<uint4*>(&sm.col_scales[0][0])[i] = make_uint4(0, 0, 0, 0);
     }
 
+    constexpr bool kRowTab = !(ROW_FMT == 1 && COL_FMT == 2);
+    __shared__ float q_tab[2][16];
+    if constexpr ((ROW_FMT == 1 && kRowTab) || COL_FMT == 1) nvfp4_fill_q_tab<ROW_FMT, COL_FMT>(a, g, q_tab);
+
     ThreadTile t;
     load_tile(a, g, prow0, k0, t);
-    __syncthreads();  // staging cleared
+    __syncthreads();  // staging cleared, q_tab filled
 
     // ---------------- rowwise direction
     if constexpr (ROW_FMT == 1) {  // NVFP4, 16-blocks = lane pair
@@ -319,7 +362,9 @@ __global__ void __launch_bounds__(kThreads, 2) quantize_kernel(QuantArgs a)
             for (int j = 0; j < 8; ++j) b = fmaxf(b, fabsf(v[j]));
             b = fmaxf(b, __shfl_xor_sync(0xFFFFFFFFu, b, 1));
             float e;
-            const uint32_t S = nvfp4_block_scale(ts, b, e);
+            uint32_t S;
+            if constexpr (kRowTab) S = nvfp4_block_scale(ts, q_tab[0], b, e);
+            else S = nvfp4_block_scale_div(ts, b, e);
             const int64_t p = prow0 + i;
             const uint64_t L0 = (uint64_t)p * (uint64_t)a.K + (uint64_t)k0;
             const uint32_t codes = nvfp4_encode8<SR>(v, e, L0, 0, a);
@@ -374,7 +419,7 @@ __global__ void __launch_bounds__(kThreads, 2) quantize_kernel(QuantArgs a)
 #pragma unroll
             for (int i = 0; i < 16; ++i) b = fmaxf(b, fabsf(u[i]));
             float e;
-            const uint32_t S = nvfp4_block_scale(ts, b, e);
+            const uint32_t S = nvfp4_block_scale(ts, q_tab[1], b, e);
             const int64_t k = k0 + j;
             const uint64_t Lbase = (uint64_t)k * (uint64_t)a.col_cols_store + (uint64_t)prow0;
             float h0[8], h1[8];
