@@ -10,10 +10,40 @@
 
 namespace nvq {
 
+// 32 accumulator columns (fp32 bits) -> alpha * acc (+ bias) as 16 bf16 pairs
+// (column 2i in the low half of out[i]); bcol: C column of v[0].
+__device__ __forceinline__ void pack32_bf16(const GemmArgs& args, const uint32_t (&v)[32], float alpha, int bcol,
+                                            uint32_t* out)
+{
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        float y0 = __fmul_rn(alpha, __uint_as_float(v[2 * i]));
+        float y1 = __fmul_rn(alpha, __uint_as_float(v[2 * i + 1]));
+        if (args.bias) {
+            y0 = __fadd_rn(y0, __uint_as_float((uint32_t)args.bias[bcol + 2 * i] << 16));
+            y1 = __fadd_rn(y1, __uint_as_float((uint32_t)args.bias[bcol + 2 * i + 1] << 16));
+        }
+        __nv_bfloat162 b2 = __floats2bfloat162_rn(y0, y1);
+        out[i] = *reinterpret_cast<uint32_t*>(&b2);
+    }
+}
+
+// 32 accumulator columns from TMEM (zero for an empty contraction).
+__device__ __forceinline__ void load32(uint32_t taddr, bool have_k, uint32_t (&v)[32])
+{
+    if (have_k) {
+        tmem_ld_32x32b_x32(taddr, v);
+        tmem_ld_wait();
+        tmem_regs_ready(v);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = 0u;
+    }
+}
+
 // Reads the warp's slice in 32-column chunks, scales, adds the bias and packs
-// to bf16 pairs (column 2i in the low half of packed[i]).  taddr: TMEM address
-// of the slice (its lane quadrant, first column); have_k: false for an empty
-// contraction (the slice is zero).
+// to bf16 pairs.  taddr: TMEM address of the slice (its lane quadrant, first
+// column); have_k: false for an empty contraction (the slice is zero).
 template <int kCols>
 __device__ __forceinline__ void pack_slice_bf16(const GemmArgs& args, uint32_t taddr, bool have_k, float alpha,
                                                 int col0, uint32_t (&packed)[kCols / 2])
@@ -21,24 +51,8 @@ __device__ __forceinline__ void pack_slice_bf16(const GemmArgs& args, uint32_t t
 #pragma unroll
     for (int c = 0; c < kCols / 32; ++c) {
         uint32_t v[32];
-        if (have_k) {
-            tmem_ld_32x32b_x32(taddr + (uint32_t)(c * 32), v);
-            tmem_ld_wait();
-        } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = 0u;
-        }
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            float y0 = __fmul_rn(alpha, __uint_as_float(v[2 * i]));
-            float y1 = __fmul_rn(alpha, __uint_as_float(v[2 * i + 1]));
-            if (args.bias) {
-                y0 = __fadd_rn(y0, __uint_as_float((uint32_t)args.bias[col0 + c * 32 + 2 * i] << 16));
-                y1 = __fadd_rn(y1, __uint_as_float((uint32_t)args.bias[col0 + c * 32 + 2 * i + 1] << 16));
-            }
-            __nv_bfloat162 b2 = __floats2bfloat162_rn(y0, y1);
-            packed[c * 16 + i] = *reinterpret_cast<uint32_t*>(&b2);
-        }
+        load32(taddr + (uint32_t)(c * 32), have_k, v);
+        pack32_bf16(args, v, alpha, col0 + c * 32, &packed[c * 16]);
     }
 }
 
@@ -77,6 +91,8 @@ __device__ __forceinline__ void epilogue_slice(const GemmArgs& args, uint32_t ta
             tmem_ld_32x32b_x32(taddr + (uint32_t)(p * 64), *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
             tmem_ld_32x32b_x32(taddr + (uint32_t)(p * 64 + 32), *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
             tmem_ld_wait();
+            tmem_regs_ready(*reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+            tmem_regs_ready(*reinterpret_cast<uint32_t(*)[32]>(&v[32]));
         } else {
 #pragma unroll
             for (int i = 0; i < 64; ++i) v[i] = 0u;
@@ -103,28 +119,42 @@ __device__ __forceinline__ void epilogue_slice(const GemmArgs& args, uint32_t ta
 // store's tensor map expects) into its staging buffer, and one lane issues a
 // bulk tensor store, so every global write is a full 128-byte line (register
 // stores write one 32-byte sector per row and instruction, and their L1
-// traffic slowed the tensor pipe).  stage: 1024-byte aligned, 4 KB, owned by
-// this warp; c_row0: C row of the slice's first row.  The lane that issues the
-// stores waits for their completion before the CTA exits.
+// traffic slowed the tensor pipe).  The TMEM loads go two chunks at a time,
+// and the first 64 columns are converted and handed to the TMA before the last
+// loads, so the accumulator is released after two load round trips instead of
+// four.  stage: 1024-byte aligned, 4 KB, owned by this warp; c_row0: C row of
+// the slice's first row.  The lane that issues the stores waits for their
+// completion before the CTA exits.
 template <int kCols, typename Release>
 __device__ __forceinline__ void epilogue_slice_tma(const GemmArgs& args, const CUtensorMap* c_map, uint8_t* stage,
                                                    uint32_t taddr, bool have_k, float alpha, int col0, int c_row0,
                                                    int lane, Release release)
 {
     static_assert(kCols % 64 == 0, "64-column granularity");
-    uint32_t packed[kCols / 2];
-    pack_slice_bf16<kCols>(args, taddr, have_k, alpha, col0, packed);
-    release();
     uint8_t* row = stage + lane * 128;
 #pragma unroll
     for (int b = 0; b < kCols / 64; ++b) {
+        uint32_t v0[32], v1[32];
+        if (have_k) {
+            tmem_ld_32x32b_x32(taddr + (uint32_t)(64 * b), v0);
+            tmem_ld_32x32b_x32(taddr + (uint32_t)(64 * b + 32), v1);
+            tmem_ld_wait();
+            tmem_regs_ready(v0);
+            tmem_regs_ready(v1);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v0[i] = v1[i] = 0u;
+        }
+        if (b == kCols / 64 - 1) release();  // every TMEM load of the slice has completed
+        uint32_t packed[32];
+        pack32_bf16(args, v0, alpha, col0 + 64 * b, &packed[0]);
+        pack32_bf16(args, v1, alpha, col0 + 64 * b + 32, &packed[16]);
         if (lane == 0) bulk_wait_group_read0();  // the previous store has read the buffer
         __syncwarp();
 #pragma unroll
         for (int c = 0; c < 8; ++c)
             *reinterpret_cast<uint4*>(row + ((c ^ (lane & 7)) << 4)) =
-                make_uint4(packed[32 * b + 4 * c], packed[32 * b + 4 * c + 1], packed[32 * b + 4 * c + 2],
-                           packed[32 * b + 4 * c + 3]);
+                make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
