@@ -237,6 +237,33 @@ NVQ_API nvq_status nvq_grouped_gemm_wgrad(const nvq_qtensor* A, const nvq_qtenso
                                   const int64_t* group_rows, int G, void* C, int64_t ldc,
                                   nvq_stream stream);
 
+/* Grouped linear layer in the recipe of the [TE] hybrid MoE example
+ * ("Hybrid quantization", Description): forward in NVFP4 (rowwise x and W),
+ * backward in MXFP8 (columnwise x and W quantized from the original bf16,
+ * dy rowwise and columnwise).  T = sum m_g tokens, G experts of N outputs
+ * and K inputs.  Compositions of the grouped calls above, on `stream`.
+ *
+ * fwd: x bf16 [T][K], w bf16 [G*N][K] (expert g = rows g*N..), y bf16
+ * [T][N].  x_row NVFP4 [P_G][K] and w_row NVFP4 [G*N][K] (G amax each) are
+ * written; saved_x_col MXFP8 [K][P_G] and saved_w_col MXFP8 [K][G*N] are
+ * written when their data is non-NULL (needed by dgrad / wgrad). */
+NVQ_API nvq_status nvq_grouped_linear_fwd(const void* x, const void* w, const int64_t* group_rows, int G,
+                                          int64_t N, int64_t K, void* y, nvq_qtensor* x_row,
+                                          nvq_qtensor* w_row, nvq_qtensor* saved_x_col,
+                                          nvq_qtensor* saved_w_col, nvq_stream stream);
+
+/* dy bf16 [T][N] -> MXFP8 dy_row [P_G][N] and dy_col [N][P_G]. */
+NVQ_API nvq_status nvq_grouped_linear_bwd_quantize(const void* dy, const int64_t* group_rows, int G, int64_t N,
+                                                   nvq_qtensor* dy_row, nvq_qtensor* dy_col, nvq_stream stream);
+
+/* dx bf16 [T][K]: dx_g = dy_g W_g for every group. */
+NVQ_API nvq_status nvq_grouped_linear_dgrad(const nvq_qtensor* dy_row, const nvq_qtensor* saved_w_col,
+                                            const int64_t* group_rows, int G, void* dx, nvq_stream stream);
+
+/* dW bf16 [G][N][K]: dW_g = dy_g^T x_g (zero for an empty group). */
+NVQ_API nvq_status nvq_grouped_linear_wgrad(const nvq_qtensor* dy_col, const nvq_qtensor* saved_x_col,
+                                            const int64_t* group_rows, int G, void* dw, nvq_stream stream);
+
 /* ------------------------------------------------------------------ */
 /* Status                                                               */
 /* ------------------------------------------------------------------ */

@@ -26,7 +26,8 @@ __all__ = [
     "alloc_qtensor", "query_sizes", "colwise_cols", "amax", "nvfp4_quantize", "mxfp8_quantize",
     "hybrid_quantize", "gemm_tn", "nvfp4_linear_fwd", "nvfp4_linear_bwd_quantize",
     "nvfp4_linear_dgrad", "nvfp4_linear_wgrad", "grouped_padded_rows", "grouped_hybrid_quantize",
-    "grouped_gemm_rows", "grouped_gemm_wgrad", "device_status", "EXPORTED_SYMBOLS",
+    "grouped_gemm_rows", "grouped_gemm_wgrad", "grouped_linear_fwd", "grouped_linear_bwd_quantize",
+    "grouped_linear_dgrad", "grouped_linear_wgrad", "device_status", "EXPORTED_SYMBOLS",
 ]
 
 NONE, NVFP4, MXFP8 = 0, 1, 2
@@ -77,6 +78,10 @@ _SIGS = {
     "nvq_grouped_hybrid_quantize": (_I32, [_P, _I64, _I64, ctypes.POINTER(_I64), _I32, _I32, _I32, _QTP, _QTP, ctypes.POINTER(_RHT), ctypes.POINTER(_SR), _P]),
     "nvq_grouped_gemm_rows": (_I32, [_QTP, _QTP, ctypes.POINTER(_I64), _I32, _I64, _I32, _P, _I64, _P]),
     "nvq_grouped_gemm_wgrad": (_I32, [_QTP, _QTP, ctypes.POINTER(_I64), _I32, _P, _I64, _P]),
+    "nvq_grouped_linear_fwd": (_I32, [_P, _P, ctypes.POINTER(_I64), _I32, _I64, _I64, _P, _QTP, _QTP, _QTP, _QTP, _P]),
+    "nvq_grouped_linear_bwd_quantize": (_I32, [_P, ctypes.POINTER(_I64), _I32, _I64, _QTP, _QTP, _P]),
+    "nvq_grouped_linear_dgrad": (_I32, [_QTP, _QTP, ctypes.POINTER(_I64), _I32, _P, _P]),
+    "nvq_grouped_linear_wgrad": (_I32, [_QTP, _QTP, ctypes.POINTER(_I64), _I32, _P, _P]),
     "nvq_status_string": (ctypes.c_char_p, [_I32]),
     "nvq_get_device_status": (_I32, [_P, ctypes.POINTER(ctypes.c_int32)]),
     "nvq_version": (ctypes.c_char_p, []),
@@ -334,6 +339,66 @@ def grouped_gemm_wgrad(A: QTensor, B: QTensor, group_rows: Sequence[int], out: O
     _check(load().nvq_grouped_gemm_wgrad(ctypes.byref(ac), ctypes.byref(bc), arr, G, _ptr(out), out.stride(-2),
                                          _stream(stream)), "nvq_grouped_gemm_wgrad")
     return out
+
+
+def grouped_linear_fwd(x: torch.Tensor, w: torch.Tensor, group_rows: Sequence[int], stream=None,
+                       y: Optional[torch.Tensor] = None, bufs=None, save_for_backward=True):
+    """Grouped (MoE) linear forward, NVFP4: x [T][K], w [G][N][K] or [G*N][K];
+    returns (y [T][N], bufs) with bufs holding x_row, w_row and, for the
+    backward, MXFP8 x_col and w_col."""
+    T, K, _ = _bf16_2d(x)
+    arr, G = _groups(group_rows)
+    w2 = w.reshape(-1, w.shape[-1])
+    N = w2.shape[0] // G
+    P = load().nvq_grouped_padded_rows(arr, G)
+    if bufs is None:
+        bufs = dict(x_row=alloc_qtensor(NVFP4, P, K, n_amax=G, device=x.device),
+                    w_row=alloc_qtensor(NVFP4, G * N, K, n_amax=G, device=x.device),
+                    x_col=alloc_qtensor(MXFP8, K, P, device=x.device) if save_for_backward else None,
+                    w_col=alloc_qtensor(MXFP8, K, G * N, device=x.device) if save_for_backward else None)
+    if y is None:
+        y = torch.empty(T, N, dtype=torch.bfloat16, device=x.device)
+    xr, wr = bufs["x_row"].c(), bufs["w_row"].c()
+    xc = bufs["x_col"].c() if bufs.get("x_col") is not None else _QT()
+    wc = bufs["w_col"].c() if bufs.get("w_col") is not None else _QT()
+    _check(load().nvq_grouped_linear_fwd(_ptr(x), _ptr(w2), arr, G, N, K, _ptr(y), ctypes.byref(xr), ctypes.byref(wr),
+                                         ctypes.byref(xc), ctypes.byref(wc), _stream(stream)), "nvq_grouped_linear_fwd")
+    return y, bufs
+
+
+def grouped_linear_bwd_quantize(dy: torch.Tensor, group_rows: Sequence[int], stream=None, bufs=None):
+    """dy [T][N] -> MXFP8 dy_row [P][N] and dy_col [N][P] (grouped)."""
+    T, N, _ = _bf16_2d(dy)
+    arr, G = _groups(group_rows)
+    P = load().nvq_grouped_padded_rows(arr, G)
+    if bufs is None:
+        bufs = dict(dy_row=alloc_qtensor(MXFP8, P, N, device=dy.device), dy_col=alloc_qtensor(MXFP8, N, P, device=dy.device))
+    r, c = bufs["dy_row"].c(), bufs["dy_col"].c()
+    _check(load().nvq_grouped_linear_bwd_quantize(_ptr(dy), arr, G, N, ctypes.byref(r), ctypes.byref(c), _stream(stream)),
+           "nvq_grouped_linear_bwd_quantize")
+    return bufs
+
+
+def grouped_linear_dgrad(dy_row: QTensor, w_col: QTensor, group_rows: Sequence[int],
+                         dx: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    arr, G = _groups(group_rows)
+    if dx is None:
+        dx = torch.empty(sum(int(v) for v in group_rows), w_col.rows, dtype=torch.bfloat16, device=dy_row.data.device)
+    a, b = dy_row.c(), w_col.c()
+    _check(load().nvq_grouped_linear_dgrad(ctypes.byref(a), ctypes.byref(b), arr, G, _ptr(dx), _stream(stream)),
+           "nvq_grouped_linear_dgrad")
+    return dx
+
+
+def grouped_linear_wgrad(dy_col: QTensor, x_col: QTensor, group_rows: Sequence[int],
+                         dw: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    arr, G = _groups(group_rows)
+    if dw is None:
+        dw = torch.empty(G, dy_col.rows, x_col.rows, dtype=torch.bfloat16, device=dy_col.data.device)
+    a, b = dy_col.c(), x_col.c()
+    _check(load().nvq_grouped_linear_wgrad(ctypes.byref(a), ctypes.byref(b), arr, G, _ptr(dw), _stream(stream)),
+           "nvq_grouped_linear_wgrad")
+    return dw
 
 
 def device_status(stream=None) -> int:

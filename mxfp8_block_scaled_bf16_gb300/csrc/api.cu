@@ -642,6 +642,48 @@ nvq_status nvq_grouped_gemm_wgrad(const nvq_qtensor* A, const nvq_qtensor* B, co
     return s;
 }
 
+nvq_status nvq_grouped_linear_fwd(const void* x, const void* w, const int64_t* group_rows, int G, int64_t N,
+                                  int64_t K, void* y, nvq_qtensor* x_row, nvq_qtensor* w_row,
+                                  nvq_qtensor* saved_x_col, nvq_qtensor* saved_w_col, nvq_stream stream)
+{
+    if (!group_rows || !x_row || !w_row || !y) return NVQ_ERR_NULL;
+    if (G < 1 || G > kMaxGroups || N <= 0 || K <= 0) return NVQ_ERR_SHAPE;
+    const bool xc = saved_x_col && saved_x_col->data, wc = saved_w_col && saved_w_col->data;
+    nvq_status s = nvq_grouped_hybrid_quantize(x, K, K, group_rows, G, NVQ_FMT_NVFP4,
+                                               xc ? NVQ_FMT_MXFP8 : NVQ_FMT_NONE, x_row, xc ? saved_x_col : nullptr,
+                                               nullptr, nullptr, stream);
+    if (s != NVQ_OK) return s;
+    int64_t w_rows[kMaxGroups];
+    for (int g = 0; g < G; ++g) w_rows[g] = N;
+    s = nvq_grouped_hybrid_quantize(w, K, K, w_rows, G, NVQ_FMT_NVFP4, wc ? NVQ_FMT_MXFP8 : NVQ_FMT_NONE, w_row,
+                                    wc ? saved_w_col : nullptr, nullptr, nullptr, stream);
+    if (s != NVQ_OK) return s;
+    return nvq_grouped_gemm_rows(x_row, w_row, group_rows, G, N, 0, y, N, stream);
+}
+
+nvq_status nvq_grouped_linear_bwd_quantize(const void* dy, const int64_t* group_rows, int G, int64_t N,
+                                           nvq_qtensor* dy_row, nvq_qtensor* dy_col, nvq_stream stream)
+{
+    if (!dy_row || !dy_col) return NVQ_ERR_NULL;
+    return nvq_grouped_hybrid_quantize(dy, N, N, group_rows, G, NVQ_FMT_MXFP8, NVQ_FMT_MXFP8, dy_row, dy_col, nullptr,
+                                       nullptr, stream);
+}
+
+nvq_status nvq_grouped_linear_dgrad(const nvq_qtensor* dy_row, const nvq_qtensor* saved_w_col,
+                                    const int64_t* group_rows, int G, void* dx, nvq_stream stream)
+{
+    if (!dy_row || !saved_w_col) return NVQ_ERR_NULL;
+    // B = W_col [K][G*N]: group g's contraction slice is columns [g*N, (g+1)*N)
+    return nvq_grouped_gemm_rows(dy_row, saved_w_col, group_rows, G, dy_row->cols, 1, dx, saved_w_col->rows, stream);
+}
+
+nvq_status nvq_grouped_linear_wgrad(const nvq_qtensor* dy_col, const nvq_qtensor* saved_x_col,
+                                    const int64_t* group_rows, int G, void* dw, nvq_stream stream)
+{
+    if (!dy_col || !saved_x_col) return NVQ_ERR_NULL;
+    return nvq_grouped_gemm_wgrad(dy_col, saved_x_col, group_rows, G, dw, saved_x_col->rows, stream);
+}
+
 const char* nvq_status_string(nvq_status s)
 {
     switch (s) {
