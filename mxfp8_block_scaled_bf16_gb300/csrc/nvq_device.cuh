@@ -1,13 +1,14 @@
 // nvq_device.cuh -- device helpers shared by the libnvq kernels (sm_103a).
 //
-// Inline PTX wrappers for mbarriers, TMA (cp.async.bulk[.tensor]) and the
-// 5th-generation tensor core (tcgen05: TMEM alloc, block-scaled MMA, smem->TMEM
-// scale copies, TMEM loads), plus the element-format conversions and the
+// Inline PTX wrappers for mbarriers, TMA (cp.async.bulk[.tensor] loads and
+// stores) and the 5th-generation tensor core (tcgen05: TMEM alloc, block-scaled
+// MMA, TMEM loads and stores), plus the element-format conversions and the
 // Philox4x32-10 generator used by stochastic rounding.
 //
 // Every wait here is bounded: a wait that runs past its time limit records
-// NVQ_ERR_TIMEOUT in the device status word and returns false, so a broken
-// pipeline ends the kernel instead of spinning forever.
+// NVQ_ERR_TIMEOUT in the device status word (or raises the CTA's abort flag,
+// for the PTX-loop wait) and gives up, so a broken pipeline ends the kernel
+// instead of spinning forever.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -53,13 +54,6 @@ __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count)
 __device__ __forceinline__ void fence_mbarrier_init()
 {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes)
-{
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
-                 "r"(bytes)
-                 : "memory");
 }
 
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar)
@@ -128,6 +122,7 @@ __device__ __forceinline__ void mbar_wait_flag(uint64_t* bar, uint32_t parity, v
 // 1 while the CTA has not aborted (read after a mbar_wait_flag).
 __device__ __forceinline__ uint32_t live_flag(volatile int* abort_flag) { return *abort_flag == 0 ? 1u : 0u; }
 
+// Arrive with an expected transaction byte count, when live != 0.
 __device__ __forceinline__ void mbar_arrive_expect_tx_if(uint64_t* bar, uint32_t bytes, uint32_t live)
 {
     asm volatile(
@@ -143,28 +138,8 @@ __device__ __forceinline__ void tma_prefetch_desc(const void* desc)
     asm volatile("prefetch.tensormap [%0];" ::"l"(desc) : "memory");
 }
 
-// 2-D tiled load of box (x = inner, y = outer) into smem, completing on bar.
-__device__ __forceinline__ void tma_load_2d(void* dst, const void* desc, uint64_t* bar, int32_t x,
-                                            int32_t y)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
-        "l"(desc), "r"(smem_u32(bar)), "r"(x), "r"(y)
-        : "memory");
-}
-
-// Untiled bulk copy global -> smem (16-byte aligned, size % 16 == 0).
-__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar)
-{
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            smem_u32(dst)),
-        "l"(src), "r"(bytes), "r"(smem_u32(bar))
-        : "memory");
-}
-
-// tma_load_2d / bulk_load issued only when live != 0.
+// 2-D tiled load of box (x = inner, y = outer) into smem, completing on bar,
+// issued only when live != 0.
 __device__ __forceinline__ void tma_load_2d_if(void* dst, const void* desc, uint64_t* bar, int32_t x, int32_t y,
                                                uint32_t live)
 {
@@ -176,6 +151,8 @@ __device__ __forceinline__ void tma_load_2d_if(void* dst, const void* desc, uint
         : "memory");
 }
 
+// Untiled bulk copy global -> smem (16-byte aligned, size % 16 == 0), completing
+// on bar, issued only when live != 0.
 __device__ __forceinline__ void bulk_load_if(void* dst, const void* src, uint32_t bytes, uint64_t* bar, uint32_t live)
 {
     asm volatile(
@@ -262,28 +239,8 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
 constexpr uint32_t kSwizzleNone = 0;
 constexpr uint32_t kSwizzle128B = 2;
 
-// 32 rows x 128 bits from smem to TMEM lanes 0..31, replicated to all four
-// lane quadrants (the block-scale factor layout the MMA reads).
-__device__ __forceinline__ void tc_cp_32x128b_warpx4(uint32_t taddr, uint64_t sdesc)
-{
-    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
-}
-
-// D(tmem) (+)= A(smem) x B(smem)^T with per-16-block E4M3 scales (NVFP4).
-__device__ __forceinline__ void tc_mma_nvf4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                            uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
-                                            uint32_t accumulate)
-{
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %6, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X"
-        " [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
-        : "memory");
-}
-
-// tc_mma_nvf4 issued only when live != 0.
+// D(tmem) (+)= A(smem) x B(smem)^T with per-16-block E4M3 scales (NVFP4),
+// issued only when live != 0; `accumulate` = 0 overwrites D.
 __device__ __forceinline__ void tc_mma_nvf4_if(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                                uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate,
                                                uint32_t live)
@@ -298,7 +255,8 @@ __device__ __forceinline__ void tc_mma_nvf4_if(uint32_t d_tmem, uint64_t a_desc,
         : "memory");
 }
 
-// tc_mma_mxf8 issued only when live != 0.
+// Same with E4M3 elements and per-32-block E8M0 scales (MXFP8), the scale byte
+// of each k-step chosen by the scale-factor id in the instruction descriptor.
 __device__ __forceinline__ void tc_mma_mxf8_if(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                                uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate,
                                                uint32_t live)
@@ -310,20 +268,6 @@ __device__ __forceinline__ void tc_mma_mxf8_if(uint32_t d_tmem, uint64_t a_desc,
         "@g tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X"
         " [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate), "r"(live)
-        : "memory");
-}
-
-// Same with E4M3 elements and per-32-block E8M0 scales (MXFP8).
-__device__ __forceinline__ void tc_mma_mxf8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                            uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
-                                            uint32_t accumulate)
-{
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %6, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X"
-        " [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
         : "memory");
 }
 
@@ -407,12 +351,6 @@ __device__ __forceinline__ uint32_t map_to_rank(const void* p, uint32_t rank)
     return r;
 }
 
-// Arrive (release, cluster scope) on an mbarrier given by its shared::cluster address.
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr)
-{
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
-}
-
 // Relaxed cluster-scope arrive, for a signal that only orders tcgen05 work:
 // the arriving thread has already waited for its TMEM stores / loads to
 // complete (tcgen05.wait::st / ::ld) and fenced them with
@@ -423,18 +361,6 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr)
 __device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr)
 {
     asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
-}
-
-// 2-D tiled load into this CTA's smem whose completion is signalled on an
-// mbarrier of either CTA of the pair (shared::cluster address).
-__device__ __forceinline__ void tma_load_2d_pair(void* dst, const void* desc, uint32_t bar_cluster_addr, int32_t x,
-                                                 int32_t y)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
-        "l"(desc), "r"(bar_cluster_addr), "r"(x), "r"(y)
-        : "memory");
 }
 
 // tma_load_2d_pair issued only when live != 0.
@@ -514,30 +440,6 @@ __device__ __forceinline__ void tc_mma_mxf8_pair_if(uint32_t d_tmem, uint64_t a_
         "@g tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X"
         " [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate), "r"(live)
-        : "memory");
-}
-
-__device__ __forceinline__ void tc_mma_nvf4_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                                 uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate)
-{
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %6, 0;\n\t"
-        "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X"
-        " [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
-        : "memory");
-}
-
-__device__ __forceinline__ void tc_mma_mxf8_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                                 uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate)
-{
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %6, 0;\n\t"
-        "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X"
-        " [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
         : "memory");
 }
 
@@ -623,28 +525,9 @@ struct Philox4 {
     uint32_t x, y, z, w;
 };
 
-__device__ __forceinline__ Philox4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3,
-                                                 uint32_t k0, uint32_t k1)
-{
-#pragma unroll
-    for (int round = 0; round < 10; ++round) {
-        if (round > 0) {
-            k0 += 0x9E3779B9u;
-            k1 += 0xBB67AE85u;
-        }
-        const uint32_t lo0 = 0xD2511F53u * c0, hi0 = __umulhi(0xD2511F53u, c0);
-        const uint32_t lo1 = 0xCD9E8D57u * c2, hi1 = __umulhi(0xCD9E8D57u, c2);
-        const uint32_t n0 = hi1 ^ c1 ^ k0, n2 = hi0 ^ c3 ^ k1;
-        c0 = n0;
-        c1 = lo1;
-        c2 = n2;
-        c3 = lo0;
-    }
-    return {c0, c1, c2, c3};
-}
-
-// Same generator with the key schedule precomputed: rk[2r], rk[2r+1] are the
-// key words of round r.
+// Philox4x32-10 (Salmon et al., SC'11) of counter (c0, c1, c2, c3) with the
+// key schedule precomputed on the host: rk[2r], rk[2r+1] are the key words of
+// round r (the key plus r Weyl increments).
 __device__ __forceinline__ Philox4 philox4x32_10_rk(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3,
                                                     const uint32_t (&rk)[20])
 {
