@@ -312,6 +312,8 @@ def run_ours(args, rank, world, local_rank):
     q_gbs = q_bytes / (q_ms * 1e-3) / 1e9
     if args.no_cpu_baseline:
         cpu_v, cpu_desc, cpu_threads = None, "skipped (--no-cpu-baseline)", 0
+    elif world > 1:
+        cpu_v, cpu_desc, cpu_threads = None, "measured at N=1 only", 0
     else:
         cpu_v, cpu_desc, cpu_threads, _ = oracle_sample(x_h, w_h, dy_h, sign)
     line = {
