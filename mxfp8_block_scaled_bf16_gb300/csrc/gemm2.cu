@@ -19,9 +19,10 @@
 //
 // Signalling (every wait bounded, as in gemm.cu):
 //   full[s]      leader: A/B bytes of both CTAs (each CTA's TMA load signals the
-//                leader's barrier, .cta_group::2);
+//                leader's barrier, .cta_group::2); for MXFP8 also the 8 scale
+//                warps' arrivals, so the MMA issuer waits on one barrier;
 //   sf_full[s]   per CTA: this CTA's block-scale tiles;
-//   sf_ready[s]  leader: the 4 scale warps of both CTAs wrote their TMEM scales;
+//   sf_ready[s]  leader (NVFP4): the 4 scale warps of both CTAs wrote their TMEM scales;
 //   empty[s]     per CTA: the leader's MMAs of stage s finished (multicast commit);
 //   acc_full     per CTA: the tile's accumulator is complete (multicast commit);
 //   acc_empty    leader: the 8 epilogue warps of both CTAs read the accumulator.
@@ -46,6 +47,14 @@ constexpr int kFirstEpiWarp = 2 + kScaleWarps;
 constexpr int kScaleLoadWarp = kFirstEpiWarp + kEpiWarps;  // block-scale copies
 constexpr int kThreads = 32 * (kScaleLoadWarp + 1);
 constexpr uint32_t kTmemCols = 512;
+
+// Scale readiness: for MXFP8 the scale warps arrive on the stage's full
+// barrier (one wait per stage in the MMA issuer, and an issue loop that steps
+// the ring position instead of recomputing it), which measured 3-7% faster;
+// for NVFP4 the same change measured 7% slower, so NVFP4 keeps a separate
+// sf_ready barrier.
+template <int FMT>
+constexpr bool kScalesOnFull = FMT == 2;
 
 // Each CTA's TMEM holds the B scales of all 256 columns (both halves of B):
 // the pair MMA reads the full B scale set from each CTA's TMEM (holding only
@@ -178,7 +187,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kStages; ++s) {
-            mbar_init(&full[s], 1);
+            mbar_init(&full[s], kScalesOnFull<FMT> ? 1 + 2 * kScaleWarps : 1);
             mbar_init(&empty[s], 1);
             mbar_init(&sf_full[s], 1);
             mbar_init(&sf_ready[s], 2 * kScaleWarps);
@@ -237,37 +246,67 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             constexpr int kMmas = C::kStageK / C::kMmaK;
             const uint64_t a_desc0 = smem_desc(smem_u32(smem + C::kA), 16, 1024, kSwizzle128B);
             const uint64_t b_desc0 = smem_desc(smem_u32(smem + C::kB), 16, 1024, kSwizzle128B);
-            uint32_t it = 0, tl_i = 0;
-            for (int t = pair; t < total; t += n_pairs, ++tl_i) {
-                const PairTile tl = decode<C::kStageK>(args, t, 0);
-                mbar_wait_flag(acc_empty, (tl_i & 1) ^ 1, abort_flag);
-                tc_fence_after();
-                for (int kb = 0; kb < tl.num_kb; ++kb, ++it) {
-                    const int s = it % C::kStages;
-                    const uint32_t par = (it / C::kStages) & 1;
-                    mbar_wait_flag(&full[s], par, abort_flag);
-                    mbar_wait_flag(&sf_ready[s], par, abort_flag);
+            if constexpr (kScalesOnFull<FMT>) {
+                // ring position carried across tiles: slot s, phase parity par,
+                // the slot's operand descriptors and its TMEM scale columns
+                uint32_t s = 0, par = 0, tl_i = 0, live = 1u;
+                uint64_t ad = a_desc0, bd = b_desc0;
+                uint32_t sfa_col = tmem_base + C::kSfCol0;
+                for (int t = pair; t < total; t += n_pairs, ++tl_i) {
+                    const PairTile tl = decode<C::kStageK>(args, t, 0);
+                    mbar_wait_flag(acc_empty, (tl_i & 1) ^ 1, abort_flag);
                     tc_fence_after();
-                    const uint32_t live = live_flag(abort_flag);
-                    const int n_mma = min(C::kStageK, tl.k_len - kb * C::kStageK) / C::kMmaK;
-                    const uint32_t sfa_col = tmem_base + C::kSfCol0 + (uint32_t)s * C::kSfColsPerStage;
-                    const uint32_t sfb_col = sfa_col + C::kSfaCols;
-                    const uint64_t ad = a_desc0 + (uint64_t)((s * kHalfTileBytes) >> 4);
-                    const uint64_t bd = b_desc0 + (uint64_t)((s * kHalfTileBytes) >> 4);
+                    for (int kb = 0; kb < tl.num_kb; ++kb) {
+                        live = mbar_wait_live(&full[s], par, abort_flag);  // A/B bytes and scales
+                        tc_fence_after();
+                        const int n_mma = min(C::kStageK, tl.k_len - kb * C::kStageK) / C::kMmaK;
+                        const uint32_t sfb_col = sfa_col + C::kSfaCols;
 #pragma unroll
-                    for (int j = 0; j < kMmas; ++j) {
-                        const uint32_t on = (j < n_mma) ? live : 0u;
-                        const uint32_t acc = (kb > 0 || j > 0) ? 1u : 0u;
-                        if constexpr (FMT == 1)
-                            tc_mma_nvf4_pair_if(tmem_base, ad + 2 * j, bd + 2 * j, make_idesc<1>(0), sfa_col + 4 * j,
-                                                sfb_col + 4 * C::kSfbHalves * j, acc, on);
-                        else
-                            tc_mma_mxf8_pair_if(tmem_base, ad + 2 * j, bd + 2 * j, make_idesc<2>((uint32_t)j), sfa_col,
+                        for (int j = 0; j < kMmas; ++j) {
+                            const uint32_t on = (j < n_mma) ? live : 0u;
+                            const uint32_t acc = (kb > 0 || j > 0) ? 1u : 0u;
+                            tc_mma_mxf8_pair_if(tmem_base, ad + 2 * j, bd + 2 * j, make_idesc<FMT>((uint32_t)j), sfa_col,
                                                 sfb_col, acc, on);
+                        }
+                        tc_commit_pair_if(&empty[s], 0x3, live);
+                        const bool wrap = s == (uint32_t)C::kStages - 1;
+                        s = wrap ? 0u : s + 1;
+                        par ^= wrap ? 1u : 0u;
+                        ad = wrap ? a_desc0 : ad + (uint64_t)(kHalfTileBytes >> 4);
+                        bd = wrap ? b_desc0 : bd + (uint64_t)(kHalfTileBytes >> 4);
+                        sfa_col = wrap ? tmem_base + C::kSfCol0 : sfa_col + C::kSfColsPerStage;
                     }
-                    tc_commit_pair_if(&empty[s], 0x3, live);
+                    tc_commit_pair_if(acc_full, 0x3, live);
                 }
-                tc_commit_pair_if(acc_full, 0x3, live_flag(abort_flag));
+            } else {  // NVFP4
+                uint32_t it = 0, tl_i = 0;
+                for (int t = pair; t < total; t += n_pairs, ++tl_i) {
+                    const PairTile tl = decode<C::kStageK>(args, t, 0);
+                    mbar_wait_flag(acc_empty, (tl_i & 1) ^ 1, abort_flag);
+                    tc_fence_after();
+                    for (int kb = 0; kb < tl.num_kb; ++kb, ++it) {
+                        const int s = it % C::kStages;
+                        const uint32_t par = (it / C::kStages) & 1;
+                        mbar_wait_flag(&full[s], par, abort_flag);
+                        mbar_wait_flag(&sf_ready[s], par, abort_flag);
+                        tc_fence_after();
+                        const uint32_t live = live_flag(abort_flag);
+                        const int n_mma = min(C::kStageK, tl.k_len - kb * C::kStageK) / C::kMmaK;
+                        const uint32_t sfa_col = tmem_base + C::kSfCol0 + (uint32_t)s * C::kSfColsPerStage;
+                        const uint32_t sfb_col = sfa_col + C::kSfaCols;
+                        const uint64_t ad = a_desc0 + (uint64_t)((s * kHalfTileBytes) >> 4);
+                        const uint64_t bd = b_desc0 + (uint64_t)((s * kHalfTileBytes) >> 4);
+#pragma unroll
+                        for (int j = 0; j < kMmas; ++j) {
+                            const uint32_t on = (j < n_mma) ? live : 0u;
+                            const uint32_t acc = (kb > 0 || j > 0) ? 1u : 0u;
+                            tc_mma_nvf4_pair_if(tmem_base, ad + 2 * j, bd + 2 * j, make_idesc<FMT>(0), sfa_col + 4 * j,
+                                                sfb_col + 4 * C::kSfbHalves * j, acc, on);
+                        }
+                        tc_commit_pair_if(&empty[s], 0x3, live);
+                    }
+                    tc_commit_pair_if(acc_full, 0x3, live_flag(abort_flag));
+                }
             }
             tc_commit_pair(mma_done, 0x1);
             mbar_wait(mma_done, 0, args.status);
@@ -310,7 +349,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) arrive_leader(&sf_ready[s], rank);
+                if (lane == 0) arrive_leader(kScalesOnFull<FMT> ? &full[s] : &sf_ready[s], rank);
             }
         }
     } else if (warp == kScaleLoadWarp) {

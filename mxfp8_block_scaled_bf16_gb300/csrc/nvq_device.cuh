@@ -119,6 +119,38 @@ __device__ __forceinline__ void mbar_wait_flag(uint64_t* bar, uint32_t parity, v
         : "memory");
 }
 
+// mbar_wait_flag that also yields the live predicate: 1 when the phase
+// completed, 0 when the wait gave up (abort flag set by another thread, or
+// the time limit, in which case it sets the flag).
+__device__ __forceinline__ uint32_t mbar_wait_live(uint64_t* bar, uint32_t parity, volatile int* abort_flag)
+{
+    uint32_t live;
+    asm volatile(
+        "{\n\t.reg .pred P1;\n\t.reg .b64 t0, t1;\n\t.reg .b32 ab;\n\t"
+        "mov.u32 %0, 1;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 P1, [%1], %2;\n\t"
+        "@P1 bra.uni DONE;\n\t"
+        "mov.u64 t0, %%globaltimer;\n\t"
+        "LOOP:\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 P1, [%1], %2;\n\t"
+        "@P1 bra.uni DONE;\n\t"
+        "ld.volatile.shared.u32 ab, [%3];\n\t"
+        "setp.ne.u32 P1, ab, 0;\n\t"
+        "@P1 bra.uni GAVEUP;\n\t"
+        "mov.u64 t1, %%globaltimer;\n\t"
+        "sub.u64 t1, t1, t0;\n\t"
+        "setp.lt.u64 P1, t1, %4;\n\t"
+        "@P1 bra.uni LOOP;\n\t"
+        "st.volatile.shared.u32 [%3], 1;\n\t"
+        "GAVEUP:\n\t"
+        "mov.u32 %0, 0;\n\t"
+        "DONE:\n\t}"
+        : "=r"(live)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(smem_u32(const_cast<int*>(abort_flag))), "l"(kWaitLimitNs)
+        : "memory");
+    return live;
+}
+
 // 1 while the CTA has not aborted (read after a mbar_wait_flag).
 __device__ __forceinline__ uint32_t live_flag(volatile int* abort_flag) { return *abort_flag == 0 ? 1u : 0u; }
 
