@@ -83,6 +83,29 @@ def test_multi_tile_and_k_tails(fmt, M, N, K):
     assert_gemm_close(y16, ref, f"fmt{fmt} {M}x{N}x{K} bf16")
 
 
+@pytest.mark.parametrize("fmt,K", [(1, 1152), (2, 896)])
+def test_more_tiles_than_sm_pairs(fmt, K):
+    """2048 x 2560 output: 80 CTA-pair tiles for at most 76 resident pairs on
+    GB300, so some pairs run a second tile and carry the stage ring (slot,
+    phase, descriptors, TMEM scale columns) across the tile boundary.  K = 1152
+    (NVFP4) is 4.5 ring stages (a ragged last stage of 2 MMAs); K = 896 (MXFP8)
+    is 7 stages, so the ring wraps inside each tile."""
+    M, N = 2048, 2560
+    a = _randn(M, K, seed=31)
+    b = _randn(N, K, seed=32, std=0.05)
+    if fmt == 1:
+        ar, _ = nvq.nvfp4_quantize(a.cuda(), nvq.DIR_ROW)
+        br, _ = nvq.nvfp4_quantize(b.cuda(), nvq.DIR_ROW)
+        ref = _nv_ref(a, b)
+    else:
+        ar, _ = nvq.mxfp8_quantize(a.cuda(), nvq.DIR_ROW)
+        br, _ = nvq.mxfp8_quantize(b.cuda(), nvq.DIR_ROW)
+        ref = _mx_ref(a, b)
+    y32 = nvq.gemm_tn(ar, br, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert_gemm_close(y32, ref, f"fmt{fmt} {M}x{N}x{K} fp32")
+
+
 def _exact_nvfp4_operand(rows, K, rng, special_block):
     """Blocks of E2M1 grid values c * s (s a power of two, block max 6 s); one
     block holds 2688 = 6 * 448 so the tensor amax is 2688 and g = A/2688 = 1."""
