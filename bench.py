@@ -42,7 +42,7 @@ FP4_OVER_BF16 = 6.0
 # current kernels on this workload (profiles/gemm_pair_nvfp4_llama3_8b_fwd.md: the
 # forward GEMM launch; profiles/quantize_nvfp4_llama3_8b.md: the six amax + quantize
 # launches of one step).  Set to None whenever those kernels change.
-GEMM_TRAFFIC_BYTES = (104.799232 + 429.168640) * 1e6
+GEMM_TRAFFIC_BYTES = (107.147776 + 430.426624) * 1e6
 QUANT_TRAFFIC_BYTES = (134.263 + 2.949 + 134.287 + 39.597 + 117.468 + 0.084
                        + 117.494 + 29.759 + 469.811 + 0.137 + 469.907 + 228.597) * 1e6
 

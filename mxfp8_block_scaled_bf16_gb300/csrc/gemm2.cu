@@ -19,10 +19,10 @@
 //
 // Signalling (every wait bounded, as in gemm.cu):
 //   full[s]      leader: A/B bytes of both CTAs (each CTA's TMA load signals the
-//                leader's barrier, .cta_group::2); for MXFP8 also the 8 scale
-//                warps' arrivals, so the MMA issuer waits on one barrier;
+//                leader's barrier, .cta_group::2) and the arrivals of the 8 scale
+//                warps of both CTAs once their TMEM scales are written, so the MMA
+//                issuer waits on one barrier per stage;
 //   sf_full[s]   per CTA: this CTA's block-scale tiles;
-//   sf_ready[s]  leader (NVFP4): the 4 scale warps of both CTAs wrote their TMEM scales;
 //   empty[s]     per CTA: the leader's MMAs of stage s finished (multicast commit);
 //   acc_full     per CTA: the tile's accumulator is complete (multicast commit);
 //   acc_empty    leader: the 8 epilogue warps of both CTAs read the accumulator.
@@ -43,18 +43,22 @@ constexpr int BN = 256;                  // MMA N = output columns per pair tile
 constexpr int kHalfTileBytes = 128 * 128;
 constexpr int kScaleWarps = 4;
 constexpr int kEpiWarps = 8;
-constexpr int kFirstEpiWarp = 2 + kScaleWarps;
-constexpr int kScaleLoadWarp = kFirstEpiWarp + kEpiWarps;  // block-scale copies
-constexpr int kThreads = 32 * (kScaleLoadWarp + 1);
+// Warp roles, by warpgroup: 0 = TMA producer (warp 0), MMA issuer (1),
+// block-scale loader (2), idle (3); 1 = scale staging (warps 4-7, lane
+// quadrant = warp & 3); 2-3 = epilogue (warps 8-15).
+constexpr int kScaleLoadWarp = 2;
+constexpr int kFirstScaleWarp = 4;
+constexpr int kFirstEpiWarp = 8;
+constexpr int kThreads = 32 * (kFirstEpiWarp + kEpiWarps);
+// Register split (setmaxnreg): warpgroups 0-1 drop to kRegsLow so the
+// epilogue warpgroups can hold a whole 128-column accumulator slice (128
+// registers) and release the accumulator after one TMEM round trip.  The two
+// shares add up to the launch allocation: 8 x 32 x 80 + 8 x 32 x 176 = 65536
+// = kThreads x 128.
+constexpr int kRegsLow = 80;
+constexpr int kRegsHigh = 176;
+static_assert(8 * 32 * kRegsLow + 8 * 32 * kRegsHigh == kThreads * 128, "register split");
 constexpr uint32_t kTmemCols = 512;
-
-// Scale readiness: for MXFP8 the scale warps arrive on the stage's full
-// barrier (one wait per stage in the MMA issuer, and an issue loop that steps
-// the ring position instead of recomputing it), which measured 3-7% faster;
-// for NVFP4 the same change measured 7% slower, so NVFP4 keeps a separate
-// sf_ready barrier.
-template <int FMT>
-constexpr bool kScalesOnFull = FMT == 2;
 
 // Each CTA's TMEM holds the B scales of all 256 columns (both halves of B):
 // the pair MMA reads the full B scale set from each CTA's TMEM (holding only
@@ -82,7 +86,7 @@ struct Cfg {
     static constexpr int kSfa = kB + kStages * kHalfTileBytes;
     static constexpr int kSfb = kSfa + kStages * kSfaBytes;
     static constexpr int kBar = kSfb + kStages * kSfbBytes;
-    static constexpr int kNumBars = 4 * kStages + 3;  // full, empty, sf_full, sf_ready, acc_full, acc_empty, done
+    static constexpr int kNumBars = 3 * kStages + 3;  // full, empty, sf_full, acc_full, acc_empty, done
     static constexpr int kMisc = kBar + kNumBars * 8;
     static constexpr int kEpi = (kMisc + 16 + 1023) / 1024 * 1024;
     static constexpr int kAlloc = kEpi + kEpiBytes + 1024;
@@ -173,8 +177,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kBar);
     uint64_t* empty = full + C::kStages;
     uint64_t* sf_full = empty + C::kStages;
-    uint64_t* sf_ready = sf_full + C::kStages;
-    uint64_t* acc_full = sf_ready + C::kStages;
+    uint64_t* acc_full = sf_full + C::kStages;
     uint64_t* acc_empty = acc_full + 1;
     uint64_t* mma_done = acc_empty + 1;
     uint32_t* tmem_ptr = reinterpret_cast<uint32_t*>(smem + C::kMisc);
@@ -187,10 +190,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kStages; ++s) {
-            mbar_init(&full[s], kScalesOnFull<FMT> ? 1 + 2 * kScaleWarps : 1);
+            mbar_init(&full[s], 1 + 2 * kScaleWarps);  // producer (+ A/B bytes) and the scale warps
             mbar_init(&empty[s], 1);
             mbar_init(&sf_full[s], 1);
-            mbar_init(&sf_ready[s], 2 * kScaleWarps);
         }
         mbar_init(acc_full, 1);
         mbar_init(acc_empty, 2 * kEpiWarps);
@@ -211,184 +213,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_ptr;
 
-    if (warp == 0) {
-        // ------------------------------------------------ TMA producer (both CTAs)
-        // Straight-line issue as in gemm.cu: PTX-loop waits, copies guarded by
-        // the CTA's live flag.
-        if (lane == 0) {
-            uint32_t it = 0, n_armed = 0;
-            const uint32_t leader = rank == 0 ? 1u : 0u;
-            for (int t = pair; t < total; t += n_pairs) {
-                const PairTile tl = decode<C::kStageK>(args, t, rank);
-                for (int kb = 0; kb < tl.num_kb; ++kb, ++it) {
-                    const int s = it % C::kStages;
-                    mbar_wait_flag(&empty[s], ((it / C::kStages) & 1) ^ 1, abort_flag);
-                    const uint32_t live = live_flag(abort_flag);
-                    const int ka = tl.a_k0 + kb * C::kStageK, kbb = tl.b_k0 + kb * C::kStageK;
-                    mbar_arrive_expect_tx_if(&full[s], 4u * kHalfTileBytes, live & leader);  // A + B of both CTAs
-                    n_armed += live;
-                    const uint32_t bar = map_to_rank(&full[s], 0);
-                    const int b_row = tl.b_row_pair + (int)rank * 128;
-                    tma_load_2d_pair_if(smem + C::kA + s * kHalfTileBytes, &a_map, bar, FMT == 1 ? ka / 2 : ka, tl.a_row, live);
-                    tma_load_2d_pair_if(smem + C::kB + s * kHalfTileBytes, &b_map, bar, FMT == 1 ? kbb / 2 : kbb, b_row, live);
-                }
-            }
-            // the leader drains the A/B copies of both CTAs (they complete on its full barriers)
-            const uint32_t n = n_armed < (uint32_t)C::kStages ? n_armed : (uint32_t)C::kStages;
-            for (uint32_t i = 0; i < n; ++i) {
-                const uint32_t k = n_armed - 1 - i;
-                if (rank == 0) mbar_wait(&full[k % C::kStages], (k / C::kStages) & 1, args.status);
-            }
-        }
-    } else if (warp == 1) {
-        // ------------------------------------------------ MMA issuer (leader CTA)
-        if (lane == 0 && rank == 0) {
-            constexpr int kMmas = C::kStageK / C::kMmaK;
-            const uint64_t a_desc0 = smem_desc(smem_u32(smem + C::kA), 16, 1024, kSwizzle128B);
-            const uint64_t b_desc0 = smem_desc(smem_u32(smem + C::kB), 16, 1024, kSwizzle128B);
-            if constexpr (kScalesOnFull<FMT>) {
-                // ring position carried across tiles: slot s, phase parity par,
-                // the slot's operand descriptors and its TMEM scale columns
-                uint32_t s = 0, par = 0, tl_i = 0, live = 1u;
-                uint64_t ad = a_desc0, bd = b_desc0;
-                uint32_t sfa_col = tmem_base + C::kSfCol0;
-                for (int t = pair; t < total; t += n_pairs, ++tl_i) {
-                    const PairTile tl = decode<C::kStageK>(args, t, 0);
-                    mbar_wait_flag(acc_empty, (tl_i & 1) ^ 1, abort_flag);
-                    tc_fence_after();
-                    for (int kb = 0; kb < tl.num_kb; ++kb) {
-                        live = mbar_wait_live(&full[s], par, abort_flag);  // A/B bytes and scales
-                        tc_fence_after();
-                        const int n_mma = min(C::kStageK, tl.k_len - kb * C::kStageK) / C::kMmaK;
-                        const uint32_t sfb_col = sfa_col + C::kSfaCols;
-#pragma unroll
-                        for (int j = 0; j < kMmas; ++j) {
-                            const uint32_t on = (j < n_mma) ? live : 0u;
-                            const uint32_t acc = (kb > 0 || j > 0) ? 1u : 0u;
-                            tc_mma_mxf8_pair_if(tmem_base, ad + 2 * j, bd + 2 * j, make_idesc<FMT>((uint32_t)j), sfa_col,
-                                                sfb_col, acc, on);
-                        }
-                        tc_commit_pair_if(&empty[s], 0x3, live);
-                        const bool wrap = s == (uint32_t)C::kStages - 1;
-                        s = wrap ? 0u : s + 1;
-                        par ^= wrap ? 1u : 0u;
-                        ad = wrap ? a_desc0 : ad + (uint64_t)(kHalfTileBytes >> 4);
-                        bd = wrap ? b_desc0 : bd + (uint64_t)(kHalfTileBytes >> 4);
-                        sfa_col = wrap ? tmem_base + C::kSfCol0 : sfa_col + C::kSfColsPerStage;
-                    }
-                    tc_commit_pair_if(acc_full, 0x3, live);
-                }
-            } else {  // NVFP4
-                uint32_t it = 0, tl_i = 0;
-                for (int t = pair; t < total; t += n_pairs, ++tl_i) {
-                    const PairTile tl = decode<C::kStageK>(args, t, 0);
-                    mbar_wait_flag(acc_empty, (tl_i & 1) ^ 1, abort_flag);
-                    tc_fence_after();
-                    for (int kb = 0; kb < tl.num_kb; ++kb, ++it) {
-                        const int s = it % C::kStages;
-                        const uint32_t par = (it / C::kStages) & 1;
-                        mbar_wait_flag(&full[s], par, abort_flag);
-                        mbar_wait_flag(&sf_ready[s], par, abort_flag);
-                        tc_fence_after();
-                        const uint32_t live = live_flag(abort_flag);
-                        const int n_mma = min(C::kStageK, tl.k_len - kb * C::kStageK) / C::kMmaK;
-                        const uint32_t sfa_col = tmem_base + C::kSfCol0 + (uint32_t)s * C::kSfColsPerStage;
-                        const uint32_t sfb_col = sfa_col + C::kSfaCols;
-                        const uint64_t ad = a_desc0 + (uint64_t)((s * kHalfTileBytes) >> 4);
-                        const uint64_t bd = b_desc0 + (uint64_t)((s * kHalfTileBytes) >> 4);
-#pragma unroll
-                        for (int j = 0; j < kMmas; ++j) {
-                            const uint32_t on = (j < n_mma) ? live : 0u;
-                            const uint32_t acc = (kb > 0 || j > 0) ? 1u : 0u;
-                            tc_mma_nvf4_pair_if(tmem_base, ad + 2 * j, bd + 2 * j, make_idesc<FMT>(0), sfa_col + 4 * j,
-                                                sfb_col + 4 * C::kSfbHalves * j, acc, on);
-                        }
-                        tc_commit_pair_if(&empty[s], 0x3, live);
-                    }
-                    tc_commit_pair_if(acc_full, 0x3, live_flag(abort_flag));
-                }
-            }
-            tc_commit_pair(mma_done, 0x1);
-            mbar_wait(mma_done, 0, args.status);
-            if (*abort_flag) record_error(args.status, kErrTimeout);
-        }
-    } else if (warp < kFirstEpiWarp) {
-        // ------------------------------------------------ scale staging (both CTAs)
-        const int q = warp & 3;
-        uint32_t it = 0;
-        bool ok = true;
-        for (int t = pair; t < total && ok; t += n_pairs) {
-            const PairTile tl = decode<C::kStageK>(args, t, rank);
-            for (int kb = 0; kb < tl.num_kb; ++kb, ++it) {
-                const int s = it % C::kStages;
-                int good = 1;
-                if (lane == 0) good = wait_or_abort(&sf_full[s], (it / C::kStages) & 1, args.status, abort_flag);
-                good = __shfl_sync(0xFFFFFFFFu, good, 0);
-                if (!good) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const int left = tl.k_len - kb * C::kStageK;
-                const int atoms = (min(C::kStageK, left) + C::kElemPerAtom - 1) / C::kElemPerAtom;
-                const uint32_t sfa_col = tmem_base + C::kSfCol0 + (uint32_t)s * C::kSfColsPerStage;
-                const uint32_t sfb_col = sfa_col + C::kSfaCols;
-                const uint32_t lane_base = (uint32_t)(q * 32) << 16;
-                const uint8_t* sfa = smem + C::kSfa + s * C::kSfaBytes + lane * 16;
-                const uint8_t* sfb = smem + C::kSfb + s * C::kSfbBytes + lane * 16;
-#pragma unroll
-                for (int j = 0; j < C::kAtomsK; ++j) {
-                    if (j < atoms) {
-                        tmem_st_32x32b_x1(sfa_col + lane_base + 4 * j + q, *reinterpret_cast<const uint32_t*>(sfa + 512 * j + 4 * q));
-#pragma unroll
-                        for (int h = 0; h < C::kSfbHalves; ++h)
-                            tmem_st_32x32b_x4(sfb_col + lane_base + 4 * (C::kSfbHalves * j + h),
-                                              *reinterpret_cast<const uint4*>(sfb + 512 * (h * C::kAtomsK + j)));
-                    }
-                }
-                tmem_st_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) arrive_leader(kScalesOnFull<FMT> ? &full[s] : &sf_ready[s], rank);
-            }
-        }
-    } else if (warp == kScaleLoadWarp) {
-        // ------------------------------------------------ block-scale loader (both CTAs)
-        // This CTA's A scale tiles and the B scale tiles of all 256 columns,
-        // on its own thread (every copy costs its issuing thread ~100 cycles).
-        if (lane == 0) {
-            uint32_t it = 0, n_armed = 0;
-            for (int t = pair; t < total; t += n_pairs) {
-                const PairTile tl = decode<C::kStageK>(args, t, rank);
-                for (int kb = 0; kb < tl.num_kb; ++kb, ++it) {
-                    const int s = it % C::kStages;
-                    mbar_wait_flag(&empty[s], ((it / C::kStages) & 1) ^ 1, abort_flag);
-                    const uint32_t live = live_flag(abort_flag);
-                    const int ka = tl.a_k0 + kb * C::kStageK, kbb = tl.b_k0 + kb * C::kStageK;
-                    const int left = tl.k_len - kb * C::kStageK;
-                    const int atoms = min(C::kAtomsK, (left + C::kElemPerAtom - 1) / C::kElemPerAtom);
-                    const uint32_t sf_bytes = (uint32_t)atoms * 512u;
-                    mbar_arrive_expect_tx_if(&sf_full[s], sf_bytes * (1 + C::kSfbHalves), live);
-                    n_armed += live;
-                    bulk_load_if(smem + C::kSfa + s * C::kSfaBytes,
-                                 args.a_scale + ((int64_t)(tl.a_row / 128) * args.a_scale_ctiles + ka / C::kElemPerAtom) * 512,
-                                 sf_bytes, &sf_full[s], live);
-#pragma unroll
-                    for (int h = 0; h < C::kSfbHalves; ++h) {
-                        const int brow = tl.b_row_pair + h * 128;
-                        bulk_load_if(smem + C::kSfb + s * C::kSfbBytes + h * C::kAtomsK * 512,
-                                     args.b_scale + ((int64_t)(brow / 128) * args.b_scale_ctiles + kbb / C::kElemPerAtom) * 512,
-                                     sf_bytes, &sf_full[s], live);
-                    }
-                }
-            }
-            const uint32_t n = n_armed < (uint32_t)C::kStages ? n_armed : (uint32_t)C::kStages;
-            for (uint32_t i = 0; i < n; ++i) {
-                const uint32_t k = n_armed - 1 - i;
-                mbar_wait(&sf_full[k % C::kStages], (k / C::kStages) & 1, args.status);
-            }
-        }
-    } else {
+    // Each role's code sits inside its warpgroups' setmaxnreg branch, so the
+    // compiler gives the epilogue the raised register budget.
+    if (warp >= kFirstEpiWarp) {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsHigh));
         // ------------------------------------------------ epilogue (both CTAs)
         constexpr int kCols = BN / 2;
         const int quad = warp & 3;
@@ -427,7 +255,160 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 epilogue_slice<kCols>(args, taddr, tl.num_kb > 0, alpha, col0, rowoff, row_ok, release);
         }
         if (lane == 0) bulk_wait_group0();  // this warp's C stores completed before the CTA exits
-    }
+    } else {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
+        if (warp == 0) {
+            // ------------------------------------------------ TMA producer (both CTAs)
+            // Straight-line issue as in gemm.cu: PTX-loop waits, copies guarded by
+            // the CTA's live flag.
+            if (lane == 0) {
+                uint32_t it = 0, n_armed = 0;
+                const uint32_t leader = rank == 0 ? 1u : 0u;
+                for (int t = pair; t < total; t += n_pairs) {
+                    const PairTile tl = decode<C::kStageK>(args, t, rank);
+                    for (int kb = 0; kb < tl.num_kb; ++kb, ++it) {
+                        const int s = it % C::kStages;
+                        mbar_wait_flag(&empty[s], ((it / C::kStages) & 1) ^ 1, abort_flag);
+                        const uint32_t live = live_flag(abort_flag);
+                        const int ka = tl.a_k0 + kb * C::kStageK, kbb = tl.b_k0 + kb * C::kStageK;
+                        mbar_arrive_expect_tx_if(&full[s], 4u * kHalfTileBytes, live & leader);  // A + B of both CTAs
+                        n_armed += live;
+                        const uint32_t bar = map_to_rank(&full[s], 0);
+                        const int b_row = tl.b_row_pair + (int)rank * 128;
+                        tma_load_2d_pair_if(smem + C::kA + s * kHalfTileBytes, &a_map, bar, FMT == 1 ? ka / 2 : ka, tl.a_row, live);
+                        tma_load_2d_pair_if(smem + C::kB + s * kHalfTileBytes, &b_map, bar, FMT == 1 ? kbb / 2 : kbb, b_row, live);
+                    }
+                }
+                // the leader drains the A/B copies of both CTAs (they complete on its full barriers)
+                const uint32_t n = n_armed < (uint32_t)C::kStages ? n_armed : (uint32_t)C::kStages;
+                for (uint32_t i = 0; i < n; ++i) {
+                    const uint32_t k = n_armed - 1 - i;
+                    if (rank == 0) mbar_wait(&full[k % C::kStages], (k / C::kStages) & 1, args.status);
+                }
+            }
+        } else if (warp == 1) {
+            // ------------------------------------------------ MMA issuer (leader CTA)
+            if (lane == 0 && rank == 0) {
+                constexpr int kMmas = C::kStageK / C::kMmaK;
+                const uint64_t a_desc0 = smem_desc(smem_u32(smem + C::kA), 16, 1024, kSwizzle128B);
+                const uint64_t b_desc0 = smem_desc(smem_u32(smem + C::kB), 16, 1024, kSwizzle128B);
+                // ring position carried across tiles: slot s, phase parity par,
+                // the slot's operand descriptors and its TMEM scale columns
+                uint32_t s = 0, par = 0, tl_i = 0, live = 1u;
+                uint64_t ad = a_desc0, bd = b_desc0;
+                uint32_t sfa_col = tmem_base + C::kSfCol0;
+                for (int t = pair; t < total; t += n_pairs, ++tl_i) {
+                    const PairTile tl = decode<C::kStageK>(args, t, 0);
+                    mbar_wait_flag(acc_empty, (tl_i & 1) ^ 1, abort_flag);
+                    tc_fence_after();
+                    for (int kb = 0; kb < tl.num_kb; ++kb) {
+                        live = mbar_wait_live(&full[s], par, abort_flag);  // A/B bytes and scales
+                        tc_fence_after();
+                        const int n_mma = min(C::kStageK, tl.k_len - kb * C::kStageK) / C::kMmaK;
+                        const uint32_t sfb_col = sfa_col + C::kSfaCols;
+#pragma unroll
+                        for (int j = 0; j < kMmas; ++j) {
+                            const uint32_t on = (j < n_mma) ? live : 0u;
+                            const uint32_t acc = (kb > 0 || j > 0) ? 1u : 0u;
+                            if constexpr (FMT == 1)
+                                tc_mma_nvf4_pair_if(tmem_base, ad + 2 * j, bd + 2 * j, make_idesc<1>(0), sfa_col + 4 * j,
+                                                    sfb_col + 4 * C::kSfbHalves * j, acc, on);
+                            else
+                                tc_mma_mxf8_pair_if(tmem_base, ad + 2 * j, bd + 2 * j, make_idesc<2>((uint32_t)j), sfa_col,
+                                                    sfb_col, acc, on);
+                        }
+                        tc_commit_pair_if(&empty[s], 0x3, live);
+                        const bool wrap = s == (uint32_t)C::kStages - 1;
+                        s = wrap ? 0u : s + 1;
+                        par ^= wrap ? 1u : 0u;
+                        ad = wrap ? a_desc0 : ad + (uint64_t)(kHalfTileBytes >> 4);
+                        bd = wrap ? b_desc0 : bd + (uint64_t)(kHalfTileBytes >> 4);
+                        sfa_col = wrap ? tmem_base + C::kSfCol0 : sfa_col + C::kSfColsPerStage;
+                    }
+                    tc_commit_pair_if(acc_full, 0x3, live);
+                }
+                tc_commit_pair(mma_done, 0x1);
+                mbar_wait(mma_done, 0, args.status);
+                if (*abort_flag) record_error(args.status, kErrTimeout);
+            }
+        } else if (warp >= kFirstScaleWarp) {
+            // ------------------------------------------------ scale staging (both CTAs)
+            const int q = warp & 3;
+            uint32_t it = 0;
+            bool ok = true;
+            for (int t = pair; t < total && ok; t += n_pairs) {
+                const PairTile tl = decode<C::kStageK>(args, t, rank);
+                for (int kb = 0; kb < tl.num_kb; ++kb, ++it) {
+                    const int s = it % C::kStages;
+                    int good = 1;
+                    if (lane == 0) good = wait_or_abort(&sf_full[s], (it / C::kStages) & 1, args.status, abort_flag);
+                    good = __shfl_sync(0xFFFFFFFFu, good, 0);
+                    if (!good) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const int left = tl.k_len - kb * C::kStageK;
+                    const int atoms = (min(C::kStageK, left) + C::kElemPerAtom - 1) / C::kElemPerAtom;
+                    const uint32_t sfa_col = tmem_base + C::kSfCol0 + (uint32_t)s * C::kSfColsPerStage;
+                    const uint32_t sfb_col = sfa_col + C::kSfaCols;
+                    const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+                    const uint8_t* sfa = smem + C::kSfa + s * C::kSfaBytes + lane * 16;
+                    const uint8_t* sfb = smem + C::kSfb + s * C::kSfbBytes + lane * 16;
+#pragma unroll
+                    for (int j = 0; j < C::kAtomsK; ++j) {
+                        if (j < atoms) {
+                            tmem_st_32x32b_x1(sfa_col + lane_base + 4 * j + q, *reinterpret_cast<const uint32_t*>(sfa + 512 * j + 4 * q));
+#pragma unroll
+                            for (int h = 0; h < C::kSfbHalves; ++h)
+                                tmem_st_32x32b_x4(sfb_col + lane_base + 4 * (C::kSfbHalves * j + h),
+                                                  *reinterpret_cast<const uint4*>(sfb + 512 * (h * C::kAtomsK + j)));
+                        }
+                    }
+                    tmem_st_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) arrive_leader(&full[s], rank);
+                }
+            }
+        } else if (warp == kScaleLoadWarp) {
+            // ------------------------------------------------ block-scale loader (both CTAs)
+            // This CTA's A scale tiles and the B scale tiles of all 256 columns,
+            // on its own thread (every copy costs its issuing thread ~100 cycles).
+            if (lane == 0) {
+                uint32_t it = 0, n_armed = 0;
+                for (int t = pair; t < total; t += n_pairs) {
+                    const PairTile tl = decode<C::kStageK>(args, t, rank);
+                    for (int kb = 0; kb < tl.num_kb; ++kb, ++it) {
+                        const int s = it % C::kStages;
+                        mbar_wait_flag(&empty[s], ((it / C::kStages) & 1) ^ 1, abort_flag);
+                        const uint32_t live = live_flag(abort_flag);
+                        const int ka = tl.a_k0 + kb * C::kStageK, kbb = tl.b_k0 + kb * C::kStageK;
+                        const int left = tl.k_len - kb * C::kStageK;
+                        const int atoms = min(C::kAtomsK, (left + C::kElemPerAtom - 1) / C::kElemPerAtom);
+                        const uint32_t sf_bytes = (uint32_t)atoms * 512u;
+                        mbar_arrive_expect_tx_if(&sf_full[s], sf_bytes * (1 + C::kSfbHalves), live);
+                        n_armed += live;
+                        bulk_load_if(smem + C::kSfa + s * C::kSfaBytes,
+                                     args.a_scale + ((int64_t)(tl.a_row / 128) * args.a_scale_ctiles + ka / C::kElemPerAtom) * 512,
+                                     sf_bytes, &sf_full[s], live);
+#pragma unroll
+                        for (int h = 0; h < C::kSfbHalves; ++h) {
+                            const int brow = tl.b_row_pair + h * 128;
+                            bulk_load_if(smem + C::kSfb + s * C::kSfbBytes + h * C::kAtomsK * 512,
+                                         args.b_scale + ((int64_t)(brow / 128) * args.b_scale_ctiles + kbb / C::kElemPerAtom) * 512,
+                                         sf_bytes, &sf_full[s], live);
+                        }
+                    }
+                }
+                const uint32_t n = n_armed < (uint32_t)C::kStages ? n_armed : (uint32_t)C::kStages;
+                for (uint32_t i = 0; i < n; ++i) {
+                    const uint32_t k = n_armed - 1 - i;
+                    mbar_wait(&sf_full[k % C::kStages], (k / C::kStages) & 1, args.status);
+                }
+            }
+        }
+    }  // warpgroups 0-1
 
     tc_fence_before();
     __syncthreads();

@@ -114,41 +114,44 @@ __device__ __forceinline__ void epilogue_slice(const GemmArgs& args, uint32_t ta
     }
 }
 
-// bf16 slice whose 32 rows are all valid, stored through the TMA: the warp
-// writes 32 rows x 64 columns (4 KB, 128-byte rows, 128B-swizzled as the
-// store's tensor map expects) into its staging buffer, and one lane issues a
-// bulk tensor store, so every global write is a full 128-byte line (register
-// stores write one 32-byte sector per row and instruction, and their L1
-// traffic slowed the tensor pipe).  The TMEM loads go two chunks at a time,
-// and the first 64 columns are converted and handed to the TMA before the last
-// loads, so the accumulator is released after two load round trips instead of
-// four.  stage: 1024-byte aligned, 4 KB, owned by this warp; c_row0: C row of
-// the slice's first row.  The lane that issues the stores waits for their
-// completion before the CTA exits.
+// bf16 slice whose 32 rows are all valid, stored through the TMA.  The
+// whole 128-column slice comes out of TMEM in one round trip (four x32 loads,
+// 128 registers: the caller runs with a raised register budget), the
+// accumulator is released, and only then are the values scaled, packed and
+// stored.  Each 64-column half is written into the warp's 4 KB staging buffer
+// (32 rows x 128 bytes, 128B-swizzled as the store's tensor map expects) and
+// leaves through one bulk tensor store, so every global write is a full
+// 128-byte line (register stores write one 32-byte sector per row and
+// instruction, and their L1 traffic slowed the tensor pipe).  stage:
+// 1024-byte aligned, 4 KB, owned by this warp; c_row0: C row of the slice's
+// first row.  The lane that issues the stores waits for their completion
+// before the CTA exits.
 template <int kCols, typename Release>
 __device__ __forceinline__ void epilogue_slice_tma(const GemmArgs& args, const CUtensorMap* c_map, uint8_t* stage,
                                                    uint32_t taddr, bool have_k, float alpha, int col0, int c_row0,
                                                    int lane, Release release)
 {
-    static_assert(kCols % 64 == 0, "64-column granularity");
+    static_assert(kCols == 128, "four 32-column chunks");
     uint8_t* row = stage + lane * 128;
+    uint32_t v[4][32];
+    if (have_k) {
 #pragma unroll
-    for (int b = 0; b < kCols / 64; ++b) {
-        uint32_t v0[32], v1[32];
-        if (have_k) {
-            tmem_ld_32x32b_x32(taddr + (uint32_t)(64 * b), v0);
-            tmem_ld_32x32b_x32(taddr + (uint32_t)(64 * b + 32), v1);
-            tmem_ld_wait();
-            tmem_regs_ready(v0);
-            tmem_regs_ready(v1);
-        } else {
+        for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(taddr + (uint32_t)(32 * c), v[c]);
+        tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v0[i] = v1[i] = 0u;
-        }
-        if (b == kCols / 64 - 1) release();  // every TMEM load of the slice has completed
+        for (int c = 0; c < 4; ++c) tmem_regs_ready(v[c]);
+    } else {
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[c][i] = 0u;
+    }
+    release();  // every TMEM load of the slice has completed
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
         uint32_t packed[32];
-        pack32_bf16(args, v0, alpha, col0 + 64 * b, &packed[0]);
-        pack32_bf16(args, v1, alpha, col0 + 64 * b + 32, &packed[16]);
+        pack32_bf16(args, v[2 * b], alpha, col0 + 64 * b, &packed[0]);
+        pack32_bf16(args, v[2 * b + 1], alpha, col0 + 64 * b + 32, &packed[16]);
         if (lane == 0) bulk_wait_group_read0();  // the previous store has read the buffer
         __syncwarp();
 #pragma unroll
