@@ -26,6 +26,7 @@ struct DeviceInit {
     std::once_flag once;
     int* status = nullptr;
     int num_sms = 0;
+    bool pair_ok = false;  // the CTA-pair kernel's register allocation is the one it was written for
     cudaError_t err = cudaSuccess;
 };
 
@@ -54,11 +55,19 @@ cudaError_t device_setup(int** status, int* num_sms = nullptr)
         d.err = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.status), g_status_word);
         if (d.err == cudaSuccess) d.err = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev);
         if (d.err == cudaSuccess) d.err = init_gemm_attributes();
-        if (d.err == cudaSuccess) d.err = init_gemm_pair_attributes();
+        if (d.err == cudaSuccess) d.err = init_gemm_pair_attributes(&d.pair_ok);
     });
     *status = d.status;
     if (num_sms) *num_sms = d.num_sms;
     return d.err;
+}
+
+// The current device's pair-kernel check (device_setup must have succeeded).
+bool device_pair_ok()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+    return g_dev[dev].pair_ok;
 }
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -295,7 +304,9 @@ nvq_status gemm_prepare(const nvq_qtensor* A, const nvq_qtensor* B, int64_t n_ou
     g->b_amax = B->amax;
     if (n_out % 128) return NVQ_ERR_SHAPE;
     g->block_n = gemm_block_n(n_out);
-    g->use_pair = (g->block_n == 256 && pair_gemm_enabled() && !debug_drop_first_load()) ? 1 : 0;
+    int* status = nullptr;
+    if (device_setup(&status) != cudaSuccess) return NVQ_ERR_CUDA;
+    g->use_pair = (g->block_n == 256 && pair_gemm_enabled() && device_pair_ok() && !debug_drop_first_load()) ? 1 : 0;
     g->any_k = (A->rows > 0 && A->cols > 0 && B->rows > 0 && B->cols > 0) ? 1 : 0;
     const int64_t eb = f == NVQ_FMT_NVFP4 ? 2 : 1;  // elements per byte
     // the pair kernel loads 128 rows of B per CTA; the single-CTA one block_n rows

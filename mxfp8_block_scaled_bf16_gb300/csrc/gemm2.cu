@@ -429,10 +429,19 @@ cudaError_t set_smem()
 
 }  // namespace gemm2
 
-cudaError_t init_gemm_pair_attributes()
+cudaError_t init_gemm_pair_attributes(bool* usable)
 {
+    *usable = false;
     cudaError_t e = gemm2::set_smem<1>();
     if (e == cudaSuccess) e = gemm2::set_smem<2>();
+    // The register split assumes the launch allocation is 128 registers per
+    // thread (kThreads x 128 = 65536).  With any other count, setmaxnreg.inc
+    // could wait for registers that never come free, so the pair kernel is
+    // then not used (the single-CTA kernel takes its GEMMs).
+    cudaFuncAttributes a1{}, a2{};
+    if (e == cudaSuccess) e = cudaFuncGetAttributes(&a1, gemm2::gemm_pair_kernel<1>);
+    if (e == cudaSuccess) e = cudaFuncGetAttributes(&a2, gemm2::gemm_pair_kernel<2>);
+    if (e == cudaSuccess) *usable = a1.numRegs == 128 && a2.numRegs == 128;
     return e;
 }
 

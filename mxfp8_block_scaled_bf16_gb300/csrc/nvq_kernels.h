@@ -107,6 +107,6 @@ cudaError_t init_gemm_attributes();
 // CTA-pair (cta_group::2) kernel for block_n == 256: 2 * min(tiles, num_sms / 2) CTAs.
 cudaError_t launch_gemm_pair(const void* a_map, const void* b_map, const void* c_map, const GemmArgs& g, int num_sms,
                              cudaStream_t s);
-cudaError_t init_gemm_pair_attributes();
+cudaError_t init_gemm_pair_attributes(bool* usable);  // usable: the pair kernel may run
 
 }  // namespace nvq
