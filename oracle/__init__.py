@@ -71,6 +71,8 @@ def _load():
                 "orc_nvfp4_g": (f32, [f32]),
                 "orc_nvfp4_quantize_rows": (None, [P, i64, i64, i64, f32, i32, i64, u32, P, P]),
                 "orc_nvfp4_quantize_cols": (None, [P, i64, i64, i64, f32, P, i32, i64, u32, P, P]),
+                "orc_nvfp4_quantize_rows_at": (None, [P, i64, i64, i64, f32, i32, i64, u32, i64, P, P]),
+                "orc_nvfp4_quantize_cols_at": (None, [P, i64, i64, i64, f32, P, i32, i64, u32, i64, i64, P, P]),
                 "orc_mxfp8_quantize_rows": (None, [P, i64, i64, i64, P, P]),
                 "orc_mxfp8_quantize_cols": (None, [P, i64, i64, i64, P, P]),
                 "orc_swizzled_size": (i64, [i64, i64]),
@@ -216,6 +218,37 @@ def nvfp4_quantize_cols(x, A: float | None = None, rht_sign=None, sr=None):
     return codes, scales, A
 
 
+def nvfp4_quantize_rows_at(x_rows, A: float, row0: int, sr=None):
+    """Rowwise NVFP4 of rows row0.. of a larger tensor whose amax is A (the
+    stochastic-rounding bits are those of the rows' positions in that tensor)."""
+    xb = _bf16_bits(x_rows)
+    M, K = xb.shape
+    codes = np.zeros((M, K // 2), np.uint8)
+    scales = np.zeros((M, K // 16), np.uint8)
+    seed, off = (sr if sr is not None else (0, 0))
+    _load().orc_nvfp4_quantize_rows_at(_p(xb), M, K, K, A, int(sr is not None), seed, off, row0,
+                                       _p(codes), _p(scales))
+    return codes, scales
+
+
+def nvfp4_quantize_cols_at(x_rows, A: float, row0: int, Mp_total: int, rht_sign=None, sr=None):
+    """Columnwise NVFP4 of rows row0.. (row0 % 16 == 0) of a larger tensor whose
+    columnwise storage has Mp_total columns and whose (transformed) amax is A:
+    returns (codes u8[K, Mp/2], compact scales u8[K, Mp/16]) for those rows."""
+    xb = _bf16_bits(x_rows)
+    M, K = xb.shape
+    if row0 % 16:
+        raise ValueError("row0 must be a multiple of 16")
+    s = _sign(rht_sign) if rht_sign is not None else None
+    nb = (M + 15) // 16
+    codes = np.zeros((K, nb * 8), np.uint8)
+    scales = np.zeros((K, nb), np.uint8)
+    seed, off = (sr if sr is not None else (0, 0))
+    _load().orc_nvfp4_quantize_cols_at(_p(xb), M, K, K, A, _p(s) if s is not None else None,
+                                       int(sr is not None), seed, off, row0, Mp_total, _p(codes), _p(scales))
+    return codes, scales
+
+
 def mxfp8_quantize_rows(x):
     xb = _bf16_bits(x)
     M, K = xb.shape
@@ -290,6 +323,18 @@ def gemm_tn_f64(A: np.ndarray, B: np.ndarray, alpha: float = 1.0, bias=None) -> 
     _load().orc_gemm_tn_f64(_p(a), _p(b), R, Cn, K, alpha, _p(bb) if bb is not None else None,
                             _p(out))
     return out
+
+
+def gemm_tn_f64_blas(A: np.ndarray, B: np.ndarray) -> np.ndarray:
+    """out[r, c] = sum_k A[r, k] B[c, k] in fp64 through numpy's matmul (a
+    library routine used as the dot-product step, for outputs too large for
+    the naive loop of gemm_tn_f64; same definition, different summation order,
+    both fp64)."""
+    a = np.ascontiguousarray(A, dtype=np.float64)
+    b = np.ascontiguousarray(B, dtype=np.float64)
+    if a.shape[1] != b.shape[1]:
+        raise ValueError("contraction lengths differ")
+    return a @ b.T
 
 
 def gemm_tn_sampled(fmt: int, a_codes, a_scales, g_a, b_codes, b_scales, g_b, K, rows, cols,

@@ -306,11 +306,13 @@ static void nvfp4_block(const float u[16], float A, const orc_sr* sr, int direct
     *scale = S;
 }
 
-/* Rowwise NVFP4: 16-blocks along K.  Outputs codes[M][K/2] (low nibble =
- * even k) and compact scales[M][K/16].  K % 16 == 0. */
-ORC_API void orc_nvfp4_quantize_rows(const uint16_t* x, int64_t M, int64_t K, int64_t ld, float A,
-                                     int sr_on, int64_t seed, uint32_t offset,
-                                     uint8_t* codes, uint8_t* scales)
+/* Rowwise NVFP4 of the M rows x[0..M) that are rows row0.. of a larger
+ * tensor with A its amax: 16-blocks along K, element (i, k) drawing its
+ * stochastic-rounding bits at linear index (row0 + i) * K + k.  Outputs
+ * codes[M][K/2] (low nibble = even k) and compact scales[M][K/16]. */
+ORC_API void orc_nvfp4_quantize_rows_at(const uint16_t* x, int64_t M, int64_t K, int64_t ld, float A,
+                                        int sr_on, int64_t seed, uint32_t offset, int64_t row0,
+                                        uint8_t* codes, uint8_t* scales)
 {
     orc_sr sr = {sr_on, seed, offset};
     int64_t nb = K / 16;
@@ -320,9 +322,44 @@ ORC_API void orc_nvfp4_quantize_rows(const uint16_t* x, int64_t M, int64_t K, in
             float u[16];
             uint8_t q[16];
             for (int t = 0; t < 16; ++t) u[t] = bf16_to_f32(x[i * ld + 16 * j + t]);
-            nvfp4_block(u, A, &sr, 0, (uint64_t)(i * K + 16 * j), q, &scales[i * nb + j]);
+            nvfp4_block(u, A, &sr, 0, (uint64_t)((row0 + i) * K + 16 * j), q, &scales[i * nb + j]);
             for (int t = 0; t < 8; ++t)
                 codes[i * (K / 2) + 8 * j + t] = (uint8_t)(q[2 * t] | (q[2 * t + 1] << 4));
+        }
+}
+
+/* Rowwise NVFP4: 16-blocks along K.  Outputs codes[M][K/2] (low nibble =
+ * even k) and compact scales[M][K/16].  K % 16 == 0. */
+ORC_API void orc_nvfp4_quantize_rows(const uint16_t* x, int64_t M, int64_t K, int64_t ld, float A,
+                                     int sr_on, int64_t seed, uint32_t offset,
+                                     uint8_t* codes, uint8_t* scales)
+{
+    orc_nvfp4_quantize_rows_at(x, M, K, ld, A, sr_on, seed, offset, 0, codes, scales);
+}
+
+/* Columnwise NVFP4 of the M rows x[0..M) that are rows row0.. (row0 % 16
+ * == 0) of a larger tensor whose columnwise storage has Mp_total columns and
+ * whose (transformed) amax is A: 16-blocks along the rows, stored transposed
+ * as codes[K][Mp/2] and compact scales[K][Mp/16], Mp = M rounded up to 16
+ * (rows beyond M are zero); element (k, i) draws its stochastic-rounding bits
+ * at linear index k * Mp_total + row0 + i.  rht_sign != NULL applies T to
+ * every block before quantizing. */
+ORC_API void orc_nvfp4_quantize_cols_at(const uint16_t* x, int64_t M, int64_t K, int64_t ld, float A,
+                                        const int8_t* rht_sign, int sr_on, int64_t seed, uint32_t offset,
+                                        int64_t row0, int64_t Mp_total, uint8_t* codes, uint8_t* scales)
+{
+    orc_sr sr = {sr_on, seed, offset};
+    int64_t nb = (M + 15) / 16, Mp = nb * 16;
+#pragma omp parallel for schedule(static)
+    for (int64_t k = 0; k < K; ++k)
+        for (int64_t j = 0; j < nb; ++j) {
+            float u[16];
+            uint8_t q[16];
+            load_col_block(x, M, ld, k, j, u);
+            if (rht_sign) orc_rht16(u, rht_sign);
+            nvfp4_block(u, A, &sr, 1, (uint64_t)(k * Mp_total + row0 + 16 * j), q, &scales[k * nb + j]);
+            for (int t = 0; t < 8; ++t)
+                codes[k * (Mp / 2) + 8 * j + t] = (uint8_t)(q[2 * t] | (q[2 * t + 1] << 4));
         }
 }
 
@@ -334,19 +371,8 @@ ORC_API void orc_nvfp4_quantize_cols(const uint16_t* x, int64_t M, int64_t K, in
                                      const int8_t* rht_sign, int sr_on, int64_t seed, uint32_t offset,
                                      uint8_t* codes, uint8_t* scales)
 {
-    orc_sr sr = {sr_on, seed, offset};
-    int64_t nb = (M + 15) / 16, Mp = nb * 16;
-#pragma omp parallel for schedule(static)
-    for (int64_t k = 0; k < K; ++k)
-        for (int64_t j = 0; j < nb; ++j) {
-            float u[16];
-            uint8_t q[16];
-            load_col_block(x, M, ld, k, j, u);
-            if (rht_sign) orc_rht16(u, rht_sign);
-            nvfp4_block(u, A, &sr, 1, (uint64_t)(k * Mp + 16 * j), q, &scales[k * nb + j]);
-            for (int t = 0; t < 8; ++t)
-                codes[k * (Mp / 2) + 8 * j + t] = (uint8_t)(q[2 * t] | (q[2 * t + 1] << 4));
-        }
+    int64_t Mp = (M + 15) / 16 * 16;
+    orc_nvfp4_quantize_cols_at(x, M, K, ld, A, rht_sign, sr_on, seed, offset, 0, Mp, codes, scales);
 }
 
 /* ------------------------------------------------------------------ */

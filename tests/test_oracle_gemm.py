@@ -85,3 +85,12 @@ def test_rht_cancels_in_wgrad_contraction():
     s2 = s.copy(); s2[:8] = -s2[:8]
     bad = np.linalg.norm(wgrad(s, s2) - ref) / np.linalg.norm(ref)
     assert good < 0.2 and bad > 0.5
+
+
+def test_blas_gemm_equals_loop_gemm():
+    """The numpy-matmul form computes the same fp64 product as the loop form
+    (only the summation order differs)."""
+    rng = np.random.default_rng(7)
+    A = rng.standard_normal((70, 96))
+    B = rng.standard_normal((33, 96))
+    np.testing.assert_allclose(oracle.gemm_tn_f64_blas(A, B), oracle.gemm_tn_f64(A, B), rtol=1e-12, atol=1e-12)

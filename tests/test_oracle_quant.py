@@ -271,3 +271,24 @@ def test_scale_swizzle_known_positions():
         pos[(r, c)] = int(np.nonzero(oracle.scale_swizzle(compact))[0][0])
     assert pos == {(0, 0): 0, (0, 1): 1, (1, 0): 16, (32, 0): 4, (96, 3): 15, (127, 3): 511,
                    (0, 4): 512, (128, 0): 1024}
+
+
+def test_offset_variants_are_slices_of_the_whole_tensor():
+    """Quantizing rows r0.. of a tensor with its amax and index offset gives
+    exactly the rows (or, columnwise, the contraction columns) of the
+    whole-tensor quantization, stochastic-rounding draws included."""
+    import torch
+    from mxfp8_block_scaled_bf16_gb300 import inputs
+    x = inputs.normal_bf16((112, 48), 1.0, torch.Generator().manual_seed(8))
+    sign = inputs.rht_sign_vector()
+    for sr in (None, (99, 3)):
+        c, s, A = oracle.nvfp4_quantize_rows(x, sr=sr)
+        for r0, n in ((0, 16), (32, 48), (96, 16), (40, 7)):
+            c2, s2 = oracle.nvfp4_quantize_rows_at(x[r0:r0 + n], A, r0, sr=sr)
+            assert np.array_equal(c[r0:r0 + n], c2) and np.array_equal(s[r0:r0 + n], s2)
+        for rht in (None, sign):
+            c, s, A = oracle.nvfp4_quantize_cols(x, rht_sign=rht, sr=sr)
+            for r0, n in ((0, 16), (32, 48), (96, 16)):
+                c2, s2 = oracle.nvfp4_quantize_cols_at(x[r0:r0 + n], A, r0, 112, rht_sign=rht, sr=sr)
+                assert np.array_equal(c[:, r0 // 2:(r0 + n) // 2], c2)
+                assert np.array_equal(s[:, r0 // 16:(r0 + n) // 16], s2)
