@@ -169,6 +169,28 @@ def oracle_sample(x, w, dy, sign, target_s=10.0):
     return STEP_FLOP / t_step / 1e12, desc, threads, t_q + t_g
 
 
+def oracle_single_thread(target_s=6.0):
+    """The same bounded oracle sample with one OpenMP thread, in a child
+    process (the thread count is fixed when the oracle library loads).
+    Returns (TFLOP/s, description) or (None, reason)."""
+    env = dict(os.environ, OMP_NUM_THREADS="1")
+    try:
+        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-child", str(target_s)],
+                           env=env, capture_output=True, text=True, timeout=600)
+        d = json.loads(r.stdout.strip().splitlines()[-1])
+        return d["value"], d["sample"]
+    except Exception as e:  # a reported baseline, never a reason to fail the bench
+        return None, f"single-thread oracle run failed: {type(e).__name__}"
+
+
+def _oracle_child(target_s):
+    from mxfp8_block_scaled_bf16_gb300 import inputs
+    x, w, dy = inputs.llama_up()
+    v, desc, threads, _ = oracle_sample(x, w, dy, inputs.rht_sign_vector(), target_s=target_s)
+    print(json.dumps({"value": v, "sample": desc, "threads": threads}), flush=True)
+    return 0
+
+
 # ---------------------------------------------------------------- reference arm
 def run_reference(args, rank, world):
     if rank != 0:
@@ -186,8 +208,11 @@ def run_reference(args, rank, world):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": STEP_FLOP / (value * 1e12) * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "nvfp4 (oracle: f32 encode, f64 GEMM)",
-            "data": "synthetic", "config": CONFIG,
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc},
+            "data": "synthetic", "config": CONFIG, "extrapolated": True,
+            "extrapolation": "each step times a bounded sample of the workload and scales it to the whole step "
+                             "(quantization by elements, GEMM tiles by FLOPs); ms_per_step is that estimate",
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc,
+                             "extrapolated": True},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
@@ -306,16 +331,20 @@ def run_ours(args, rank, world, local_rank):
     if rank != 0:
         return 0
     peaks, src = _peaks()
-    peak_fp4 = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")) * FP4_OVER_BF16
+    # The GEMM launch times come from a short eager pass (a few ms of GEMMs between
+    # idle gaps), not from a seconds-long loop, so the burst bf16 figure applies.
+    peak_fp4 = peaks["bf16_tflops"] * FP4_OVER_BF16
     achieved = GEMM_FLOP / (avg_gemm_ms * 1e-3) / 1e12
     q_bytes = (M * K + N * K + M * N) * 5.125  # 2 reads of bf16 + 2 x (codes + scales) writes
     q_gbs = q_bytes / (q_ms * 1e-3) / 1e9
+    st_v, st_desc = None, "not measured"
     if args.no_cpu_baseline:
         cpu_v, cpu_desc, cpu_threads = None, "skipped (--no-cpu-baseline)", 0
     elif world > 1:
         cpu_v, cpu_desc, cpu_threads = None, "measured at N=1 only", 0
     else:
         cpu_v, cpu_desc, cpu_threads, _ = oracle_sample(x_h, w_h, dy_h, sign)
+        st_v, st_desc = oracle_single_thread()
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
@@ -325,7 +354,10 @@ def run_ours(args, rank, world, local_rank):
         "roofline": {"bound": "tensor", "kernel": "gemm_pair_kernel<NVFP4> (CTA pair; fwd, dgrad, wgrad)",
                      "achieved": achieved, "peak": peak_fp4, "unit": "TFLOP/s", "frac": achieved / peak_fp4,
                      "traffic": GEMM_TRAFFIC_BYTES, "traffic_note": "bytes per launch, ncu capture of the forward GEMM",
-                     "peak_note": f"{src} bf16 sustained x {FP4_OVER_BF16} (fp4/bf16 nominal dense ratio)"},
+                     "peak_note": f"{src} bf16 burst x {FP4_OVER_BF16} (fp4/bf16 nominal dense ratio); the GEMMs "
+                                  "are timed in a short eager pass, so the burst figure applies",
+                     "frac_of_sustained": achieved / (peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+                                                      * FP4_OVER_BF16)},
         "roofline_quantize": {"bound": "hbm", "achieved": q_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                               "frac": q_gbs / peaks["hbm_gbs"], "traffic": QUANT_TRAFFIC_BYTES,
                               "traffic_note": "bytes per step (x, W, dy amax + quantize), ncu captures",
@@ -333,7 +365,10 @@ def run_ours(args, rank, world, local_rank):
         "breakdown_ms": {"step": ms_max, "gemm_fwd": statistics.mean(gemm_ms), "gemm_dgrad": statistics.mean(dgrad_ms),
                          "gemm_wgrad": statistics.mean(wgrad_ms), "quantize_x_w_dy": q_ms},
         "clocks": clk,
-        "cpu_baseline": {"value": cpu_v, "unit": UNIT, "cores": cpu_threads, "kind": "oracle", "sample": cpu_desc},
+        "cpu_baseline": {"value": cpu_v, "unit": UNIT, "cores": cpu_threads, "kind": "oracle", "sample": cpu_desc,
+                         "extrapolated": cpu_v is not None,
+                         "single_thread": {"value": st_v, "unit": UNIT, "cores": 1, "sample": st_desc,
+                                           "extrapolated": st_v is not None}},
         "e2e": e2e,
     }
     print(json.dumps(line), flush=True)
@@ -760,10 +795,13 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end measurement")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip timing the CPU oracle")
     ap.add_argument("--eager", action="store_true", help="launch the step eagerly instead of replaying a CUDA graph")
+    ap.add_argument("--oracle-child", type=float, default=None, help=argparse.SUPPRESS)
     ap.add_argument("--workload", default="llama_up",
                     choices=["llama_up", "quant_sweep", "moe_grouped", "qwen3_stack", "single_linear"],
                     help="llama_up (default: the headline line) or one of the other configurations")
     args = ap.parse_args()
+    if args.oracle_child is not None:
+        return _oracle_child(args.oracle_child)
     args.warmup = max(args.warmup, 3) if args.impl == "ours" else args.warmup
     world = _env_int("WORLD_SIZE", 1)
     rank = _env_int("RANK", 0)

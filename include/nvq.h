@@ -137,10 +137,32 @@ NVQ_API nvq_status nvq_amax(const void* x, int64_t M, int64_t K, int64_t ld, con
  * the Hadamard transform to the columnwise blocks (its amax is then taken
  * over T(x)); sr (NULL = round to nearest) applies to both directions.
  * Runs the amax pass then one fused pass that reads x once for both
- * directions; writes row->amax[0] and col->amax[0]. */
+ * directions; writes row->amax[0] and col->amax[0].
+ * Domain: x finite.  The transform adds up to 16 magnitudes in fp32, so with
+ * rht_col every |x| <= FLT_MAX / 16 keeps it finite.  Where the transform of
+ * some columnwise block overflows, the call still completes with no device
+ * error and writes every output byte: col->amax[0] is +inf and the
+ * columnwise codes and scales are unspecified; the rowwise direction does not
+ * use the transform and is unaffected. */
 NVQ_API nvq_status nvq_nvfp4_quantize(const void* x, int64_t M, int64_t K, int64_t ld, int dirs,
                               const nvq_rht* rht_col, const nvq_sr* sr, nvq_qtensor* row,
                               nvq_qtensor* col, nvq_stream stream);
+
+/* Flags of the _ex entry points. */
+enum {
+    /* The NVFP4 tensor amax is given instead of measured: row->amax[0] holds
+     * max |x| and col->amax[0] holds max |x| (or, with rht_col, the
+     * Hadamard-domain max |T(u)| over the columnwise 16-blocks) before the
+     * call, as the producer of x wrote them (nvq_gemm_tn_amax); the amax pass
+     * is skipped and x is read once.  The codes equal those of the measured
+     * call when the given amaxes equal the measured ones. */
+    NVQ_AMAX_GIVEN = 1
+};
+
+/* nvq_nvfp4_quantize with flags (NVQ_AMAX_GIVEN or 0). */
+NVQ_API nvq_status nvq_nvfp4_quantize_ex(const void* x, int64_t M, int64_t K, int64_t ld, int dirs,
+                                         const nvq_rht* rht_col, const nvq_sr* sr, int flags, nvq_qtensor* row,
+                                         nvq_qtensor* col, nvq_stream stream);
 
 /* MXFP8 quantization of bf16 x[M][K] ([TE]): E8M0 scale 2^e per 32-block,
  * e = floor(log2 amax_block) - 8 clamped to [-127, 127], elements
@@ -168,6 +190,21 @@ NVQ_API nvq_status nvq_hybrid_quantize(const void* x, int64_t M, int64_t K, int6
 NVQ_API nvq_status nvq_gemm_tn(const nvq_qtensor* A, const nvq_qtensor* B, const void* bias, void* C,
                        int64_t ldc, int c_fp32, nvq_stream stream);
 
+/* nvq_gemm_tn that also writes the amaxes of its stored output C (the values
+ * after rounding to C's type), for the quantizer of the operation that reads
+ * C next, which can then skip its amax pass (NVQ_AMAX_GIVEN; [TT] "What
+ * changed": every NVFP4 input needs its FP32 per-tensor scale):
+ *   c_amax[0]     = max |C|                                  (NULL: not computed);
+ *   c_amax_rht[0] = max |T(u)| over the 16-row column blocks u of C, T the
+ *                   Hadamard transform of nvq_rht with the sign vector rht
+ *                   (the amax the columnwise NVFP4 quantization of C with
+ *                   that sign vector needs; NULL: not computed).
+ * Both are overwritten (zeroed on the stream first).  C's rows are a
+ * multiple of 128, so every 16-row block is whole. */
+NVQ_API nvq_status nvq_gemm_tn_amax(const nvq_qtensor* A, const nvq_qtensor* B, const void* bias, void* C,
+                                    int64_t ldc, int c_fp32, const nvq_rht* rht, float* c_amax, float* c_amax_rht,
+                                    nvq_stream stream);
+
 /* NVFP4 linear forward ([TT] NVFP4Linear): quantizes x[M][K] rowwise (RTN)
  * into x_row and columnwise with the Hadamard transform into saved_x_col
  * (the wgrad operand, kept for backward); quantizes W[N][K] rowwise into
@@ -179,6 +216,16 @@ NVQ_API nvq_status nvq_nvfp4_linear_fwd(const void* x, const void* w, const void
                                 nvq_qtensor* x_row, nvq_qtensor* w_row, nvq_qtensor* saved_x_col,
                                 nvq_qtensor* saved_w_col, nvq_stream stream);
 
+/* nvq_nvfp4_linear_fwd for a layer inside a stack: flags = NVQ_AMAX_GIVEN
+ * takes x's amaxes from x_row->amax[0] and saved_x_col->amax[0] (written by
+ * the previous layer's GEMM) instead of measuring them; y_amax / y_amax_rht
+ * (NULL to skip) receive y's amaxes as nvq_gemm_tn_amax defines them, for the
+ * next layer's quantization of y. */
+NVQ_API nvq_status nvq_nvfp4_linear_fwd_ex(const void* x, const void* w, const void* bias, int64_t M, int64_t N,
+                                           int64_t K, const nvq_rht* rht, int flags, void* y, float* y_amax,
+                                           float* y_amax_rht, nvq_qtensor* x_row, nvq_qtensor* w_row,
+                                           nvq_qtensor* saved_x_col, nvq_qtensor* saved_w_col, nvq_stream stream);
+
 /* Backward quantization of dy[M][N]: rowwise (for dgrad) and columnwise with
  * the Hadamard transform (for wgrad), both with stochastic rounding. */
 NVQ_API nvq_status nvq_nvfp4_linear_bwd_quantize(const void* dy, int64_t M, int64_t N,
@@ -186,9 +233,21 @@ NVQ_API nvq_status nvq_nvfp4_linear_bwd_quantize(const void* dy, int64_t M, int6
                                          nvq_qtensor* dy_row, nvq_qtensor* dy_col,
                                          nvq_stream stream);
 
+/* nvq_nvfp4_linear_bwd_quantize with flags (NVQ_AMAX_GIVEN: dy's amaxes were
+ * written into dy_row->amax[0] / dy_col->amax[0] by the GEMM that produced dy). */
+NVQ_API nvq_status nvq_nvfp4_linear_bwd_quantize_ex(const void* dy, int64_t M, int64_t N, const nvq_rht* rht,
+                                                    const nvq_sr* sr, int flags, nvq_qtensor* dy_row,
+                                                    nvq_qtensor* dy_col, nvq_stream stream);
+
 /* dgrad: dx[M][K] = dy W = TN(dy_row [M][N], saved_w_col [K][N]), bf16. */
 NVQ_API nvq_status nvq_nvfp4_linear_dgrad(const nvq_qtensor* dy_row, const nvq_qtensor* saved_w_col,
                                   void* dx, nvq_stream stream);
+
+/* dgrad that also writes dx's amaxes (nvq_gemm_tn_amax; NULL to skip), for the
+ * quantization of dx as the output gradient of the layer below. */
+NVQ_API nvq_status nvq_nvfp4_linear_dgrad_ex(const nvq_qtensor* dy_row, const nvq_qtensor* saved_w_col,
+                                             const nvq_rht* rht, void* dx, float* dx_amax, float* dx_amax_rht,
+                                             nvq_stream stream);
 
 /* wgrad: dW[N][K] = dy^T x = TN(dy_col [N][M], saved_x_col [K][M]), bf16;
  * the Hadamard transforms cancel because both operands share one sign vector. */
@@ -273,6 +332,15 @@ NVQ_API const char* nvq_status_string(nvq_status s);
  * first device-side error recorded since the last call) in *code and
  * clears it. */
 NVQ_API nvq_status nvq_get_device_status(nvq_stream stream, int32_t* code);
+
+/* Which GEMM kernel takes the GEMMs whose output width is a multiple of 256
+ * on the current device: 1 = the CTA-pair kernel (tcgen05 cta_group::2),
+ * 0 = the single-CTA kernel (the pair kernel is disabled by NVQ_GEMM_PAIR=0,
+ * or its compiled register allocation is not the one its register split
+ * needs), -1 = the device could not be set up.  Widths that are not a
+ * multiple of 256 always take the single-CTA kernel.  Performs the library's
+ * one-time per-device set-up if it has not run yet. */
+NVQ_API int nvq_gemm_pair_available(void);
 
 /* Library version string. */
 NVQ_API const char* nvq_version(void);

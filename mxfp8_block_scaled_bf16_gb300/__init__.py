@@ -22,16 +22,18 @@ import torch
 from . import build as _build
 
 __all__ = [
-    "NVFP4", "MXFP8", "NONE", "DIR_ROW", "DIR_COL", "NvqError", "QTensor", "lib", "load",
+    "NVFP4", "MXFP8", "NONE", "DIR_ROW", "DIR_COL", "AMAX_GIVEN", "NvqError", "QTensor", "lib", "load",
     "alloc_qtensor", "query_sizes", "colwise_cols", "amax", "nvfp4_quantize", "mxfp8_quantize",
     "hybrid_quantize", "gemm_tn", "nvfp4_linear_fwd", "nvfp4_linear_bwd_quantize",
     "nvfp4_linear_dgrad", "nvfp4_linear_wgrad", "grouped_padded_rows", "grouped_hybrid_quantize",
     "grouped_gemm_rows", "grouped_gemm_wgrad", "grouped_linear_fwd", "grouped_linear_bwd_quantize",
-    "grouped_linear_dgrad", "grouped_linear_wgrad", "device_status", "EXPORTED_SYMBOLS",
+    "grouped_linear_dgrad", "grouped_linear_wgrad", "device_status", "gemm_pair_available",
+    "EXPORTED_SYMBOLS",
 ]
 
 NONE, NVFP4, MXFP8 = 0, 1, 2
 DIR_ROW, DIR_COL = 1, 2
+AMAX_GIVEN = 1
 MAX_GROUPS = 256
 
 STATUS_NAMES = {0: "NVQ_OK", 1: "NVQ_ERR_NULL", 2: "NVQ_ERR_SHAPE", 3: "NVQ_ERR_ALIGN",
@@ -67,12 +69,19 @@ _SIGS = {
     "nvq_colwise_cols": (_I64, [_I32, _I64]),
     "nvq_amax": (_I32, [_P, _I64, _I64, _I64, ctypes.POINTER(_RHT), _P, _P, _P]),
     "nvq_nvfp4_quantize": (_I32, [_P, _I64, _I64, _I64, _I32, ctypes.POINTER(_RHT), ctypes.POINTER(_SR), _QTP, _QTP, _P]),
+    "nvq_nvfp4_quantize_ex": (_I32, [_P, _I64, _I64, _I64, _I32, ctypes.POINTER(_RHT), ctypes.POINTER(_SR), _I32, _QTP, _QTP, _P]),
     "nvq_mxfp8_quantize": (_I32, [_P, _I64, _I64, _I64, _I32, _QTP, _QTP, _P]),
     "nvq_hybrid_quantize": (_I32, [_P, _I64, _I64, _I64, _I32, _I32, _I32, ctypes.POINTER(_RHT), ctypes.POINTER(_SR), _QTP, _QTP, _P]),
     "nvq_gemm_tn": (_I32, [_QTP, _QTP, _P, _P, _I64, _I32, _P]),
+    "nvq_gemm_tn_amax": (_I32, [_QTP, _QTP, _P, _P, _I64, _I32, ctypes.POINTER(_RHT), _P, _P, _P]),
     "nvq_nvfp4_linear_fwd": (_I32, [_P, _P, _P, _I64, _I64, _I64, ctypes.POINTER(_RHT), _P, _QTP, _QTP, _QTP, _QTP, _P]),
+    "nvq_nvfp4_linear_fwd_ex": (_I32, [_P, _P, _P, _I64, _I64, _I64, ctypes.POINTER(_RHT), _I32, _P, _P, _P, _QTP, _QTP,
+                                       _QTP, _QTP, _P]),
     "nvq_nvfp4_linear_bwd_quantize": (_I32, [_P, _I64, _I64, ctypes.POINTER(_RHT), ctypes.POINTER(_SR), _QTP, _QTP, _P]),
+    "nvq_nvfp4_linear_bwd_quantize_ex": (_I32, [_P, _I64, _I64, ctypes.POINTER(_RHT), ctypes.POINTER(_SR), _I32, _QTP,
+                                                _QTP, _P]),
     "nvq_nvfp4_linear_dgrad": (_I32, [_QTP, _QTP, _P, _P]),
+    "nvq_nvfp4_linear_dgrad_ex": (_I32, [_QTP, _QTP, ctypes.POINTER(_RHT), _P, _P, _P, _P]),
     "nvq_nvfp4_linear_wgrad": (_I32, [_QTP, _QTP, _P, _P]),
     "nvq_grouped_padded_rows": (_I64, [ctypes.POINTER(_I64), _I32]),
     "nvq_grouped_hybrid_quantize": (_I32, [_P, _I64, _I64, ctypes.POINTER(_I64), _I32, _I32, _I32, _QTP, _QTP, ctypes.POINTER(_RHT), ctypes.POINTER(_SR), _P]),
@@ -84,6 +93,7 @@ _SIGS = {
     "nvq_grouped_linear_wgrad": (_I32, [_QTP, _QTP, ctypes.POINTER(_I64), _I32, _P, _P]),
     "nvq_status_string": (ctypes.c_char_p, [_I32]),
     "nvq_get_device_status": (_I32, [_P, ctypes.POINTER(ctypes.c_int32)]),
+    "nvq_gemm_pair_available": (_I32, []),
     "nvq_version": (ctypes.c_char_p, []),
 }
 EXPORTED_SYMBOLS = tuple(_SIGS)
@@ -208,14 +218,17 @@ def hybrid_quantize(x: torch.Tensor, row_fmt: int, col_fmt: int, rht_sign=None, 
 
 
 def nvfp4_quantize(x: torch.Tensor, dirs: int = DIR_ROW | DIR_COL, rht_sign=None, sr=None, stream=None,
-                   out_row: Optional[QTensor] = None, out_col: Optional[QTensor] = None):
+                   out_row: Optional[QTensor] = None, out_col: Optional[QTensor] = None, amax_given: bool = False):
+    """NVFP4 row and/or column quantization.  amax_given: the outputs' amax
+    buffers already hold x's amaxes (written by the GEMM that produced x), so
+    the amax pass is skipped."""
     M, K, ld = _bf16_2d(x)
     row = out_row or (alloc_qtensor(NVFP4, M, K, device=x.device) if dirs & DIR_ROW else None)
     col = out_col or (alloc_qtensor(NVFP4, K, colwise_cols(NVFP4, M), device=x.device) if dirs & DIR_COL else None)
     rc, cc = (row.c() if row else None), (col.c() if col else None)
-    _check(load().nvq_nvfp4_quantize(_ptr(x), M, K, ld, dirs, _rht(rht_sign), _sr(sr),
-                                     ctypes.byref(rc) if rc else None, ctypes.byref(cc) if cc else None,
-                                     _stream(stream)), "nvq_nvfp4_quantize")
+    _check(load().nvq_nvfp4_quantize_ex(_ptr(x), M, K, ld, dirs, _rht(rht_sign), _sr(sr), AMAX_GIVEN if amax_given else 0,
+                                        ctypes.byref(rc) if rc else None, ctypes.byref(cc) if cc else None,
+                                        _stream(stream)), "nvq_nvfp4_quantize_ex")
     return row, col
 
 
@@ -231,20 +244,32 @@ def mxfp8_quantize(x: torch.Tensor, dirs: int = DIR_ROW | DIR_COL, stream=None,
 
 
 def gemm_tn(A: QTensor, B: QTensor, bias: Optional[torch.Tensor] = None, out_dtype=torch.bfloat16,
-            out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
-    """C[r, c] = alpha * sum_k A[r, k] B[c, k] (+ bias[c])."""
+            out: Optional[torch.Tensor] = None, stream=None, rht_sign=None, amax_out: Optional[torch.Tensor] = None,
+            amax_rht_out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """C[r, c] = alpha * sum_k A[r, k] B[c, k] (+ bias[c]).  amax_out /
+    amax_rht_out (fp32 device tensors, element 0 written): the plain and
+    Hadamard-domain (sign vector rht_sign) amaxes of the stored C."""
     if out is None:
         out = torch.empty(A.rows, B.rows, dtype=out_dtype, device=A.data.device)
     ac, bc = A.c(), B.c()
-    _check(load().nvq_gemm_tn(ctypes.byref(ac), ctypes.byref(bc), _ptr(bias), _ptr(out), out.stride(0),
-                              1 if out.dtype == torch.float32 else 0, _stream(stream)), "nvq_gemm_tn")
+    c32 = 1 if out.dtype == torch.float32 else 0
+    if amax_out is None and amax_rht_out is None:
+        _check(load().nvq_gemm_tn(ctypes.byref(ac), ctypes.byref(bc), _ptr(bias), _ptr(out), out.stride(0), c32,
+                                  _stream(stream)), "nvq_gemm_tn")
+    else:
+        _check(load().nvq_gemm_tn_amax(ctypes.byref(ac), ctypes.byref(bc), _ptr(bias), _ptr(out), out.stride(0), c32,
+                                       _rht(rht_sign), _ptr(amax_out), _ptr(amax_rht_out), _stream(stream)),
+               "nvq_gemm_tn_amax")
     return out
 
 
 def nvfp4_linear_fwd(x: torch.Tensor, w: torch.Tensor, bias=None, rht_sign=None, save_for_backward=True,
-                     stream=None, y: Optional[torch.Tensor] = None, bufs=None):
+                     stream=None, y: Optional[torch.Tensor] = None, bufs=None, amax_given: bool = False,
+                     y_amax: Optional[torch.Tensor] = None, y_amax_rht: Optional[torch.Tensor] = None):
     """y = x W^T with NVFP4 operands; returns (y, saved) where saved holds the
-    quantized x_row, w_row, the RHT'd columnwise x (wgrad) and columnwise W (dgrad)."""
+    quantized x_row, w_row, the RHT'd columnwise x (wgrad) and columnwise W (dgrad).
+    amax_given: bufs["x_row"].amax / bufs["x_col"].amax already hold x's
+    amaxes; y_amax / y_amax_rht receive y's amaxes for the next layer."""
     M, K, _ = _bf16_2d(x)
     N = w.shape[0]
     if bufs is None:
@@ -257,29 +282,34 @@ def nvfp4_linear_fwd(x: torch.Tensor, w: torch.Tensor, bias=None, rht_sign=None,
     xr, wr = bufs["x_row"].c(), bufs["w_row"].c()
     xc = bufs["x_col"].c() if bufs.get("x_col") is not None else _QT()
     wc = bufs["w_col"].c() if bufs.get("w_col") is not None else _QT()
-    _check(load().nvq_nvfp4_linear_fwd(_ptr(x), _ptr(w), _ptr(bias), M, N, K, _rht(rht_sign), _ptr(y),
-                                       ctypes.byref(xr), ctypes.byref(wr), ctypes.byref(xc), ctypes.byref(wc),
-                                       _stream(stream)), "nvq_nvfp4_linear_fwd")
+    _check(load().nvq_nvfp4_linear_fwd_ex(_ptr(x), _ptr(w), _ptr(bias), M, N, K, _rht(rht_sign),
+                                          AMAX_GIVEN if amax_given else 0, _ptr(y), _ptr(y_amax), _ptr(y_amax_rht),
+                                          ctypes.byref(xr), ctypes.byref(wr), ctypes.byref(xc), ctypes.byref(wc),
+                                          _stream(stream)), "nvq_nvfp4_linear_fwd_ex")
     return y, bufs
 
 
-def nvfp4_linear_bwd_quantize(dy: torch.Tensor, rht_sign=None, sr=None, stream=None, bufs=None):
+def nvfp4_linear_bwd_quantize(dy: torch.Tensor, rht_sign=None, sr=None, stream=None, bufs=None,
+                              amax_given: bool = False):
     M, N, _ = _bf16_2d(dy)
     if bufs is None:
         bufs = dict(dy_row=alloc_qtensor(NVFP4, M, N, device=dy.device),
                     dy_col=alloc_qtensor(NVFP4, N, colwise_cols(NVFP4, M), device=dy.device))
     r, c = bufs["dy_row"].c(), bufs["dy_col"].c()
-    _check(load().nvq_nvfp4_linear_bwd_quantize(_ptr(dy), M, N, _rht(rht_sign), _sr(sr), ctypes.byref(r),
-                                                ctypes.byref(c), _stream(stream)), "nvq_nvfp4_linear_bwd_quantize")
+    _check(load().nvq_nvfp4_linear_bwd_quantize_ex(_ptr(dy), M, N, _rht(rht_sign), _sr(sr),
+                                                   AMAX_GIVEN if amax_given else 0, ctypes.byref(r), ctypes.byref(c),
+                                                   _stream(stream)), "nvq_nvfp4_linear_bwd_quantize_ex")
     return bufs
 
 
-def nvfp4_linear_dgrad(dy_row: QTensor, w_col: QTensor, dx: Optional[torch.Tensor] = None, stream=None):
+def nvfp4_linear_dgrad(dy_row: QTensor, w_col: QTensor, dx: Optional[torch.Tensor] = None, stream=None,
+                       rht_sign=None, dx_amax: Optional[torch.Tensor] = None,
+                       dx_amax_rht: Optional[torch.Tensor] = None):
     if dx is None:
         dx = torch.empty(dy_row.rows, w_col.rows, dtype=torch.bfloat16, device=dy_row.data.device)
     a, b = dy_row.c(), w_col.c()
-    _check(load().nvq_nvfp4_linear_dgrad(ctypes.byref(a), ctypes.byref(b), _ptr(dx), _stream(stream)),
-           "nvq_nvfp4_linear_dgrad")
+    _check(load().nvq_nvfp4_linear_dgrad_ex(ctypes.byref(a), ctypes.byref(b), _rht(rht_sign), _ptr(dx), _ptr(dx_amax),
+                                            _ptr(dx_amax_rht), _stream(stream)), "nvq_nvfp4_linear_dgrad_ex")
     return dx
 
 
@@ -399,6 +429,14 @@ def grouped_linear_wgrad(dy_col: QTensor, x_col: QTensor, group_rows: Sequence[i
     _check(load().nvq_grouped_linear_wgrad(ctypes.byref(a), ctypes.byref(b), arr, G, _ptr(dw), _stream(stream)),
            "nvq_grouped_linear_wgrad")
     return dw
+
+
+def gemm_pair_available() -> bool:
+    """True when GEMMs with an output width divisible by 256 run on the CTA-pair kernel."""
+    v = load().nvq_gemm_pair_available()
+    if v < 0:
+        raise NvqError(6, "nvq_gemm_pair_available")
+    return v == 1
 
 
 def device_status(stream=None) -> int:

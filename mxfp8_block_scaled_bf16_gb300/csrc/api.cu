@@ -146,7 +146,7 @@ uint32_t sign_mask(const nvq_rht* rht, bool* ok)
 // of M rows (outputs unpadded: row rows = M, col cols = colwise_cols(M)).
 nvq_status quantize_impl(const void* x, int64_t M, int64_t K, int64_t ld, const int64_t* group_rows, int G,
                          nvq_format row_fmt, nvq_format col_fmt, const nvq_rht* rht_col, const nvq_sr* sr,
-                         nvq_qtensor* row, nvq_qtensor* col, cudaStream_t stream)
+                         nvq_qtensor* row, nvq_qtensor* col, cudaStream_t stream, bool amax_given = false)
 {
     if (row_fmt != NVQ_FMT_NONE && !valid_fmt(row_fmt)) return NVQ_ERR_UNSUPPORTED;
     if (col_fmt != NVQ_FMT_NONE && !valid_fmt(col_fmt)) return NVQ_ERR_UNSUPPORTED;
@@ -250,7 +250,7 @@ nvq_status quantize_impl(const void* x, int64_t M, int64_t K, int64_t ld, const 
         }
         return cuda_status(e);
     }
-    if (any_nv) {
+    if (any_nv && !amax_given) {
         // amax pass: plain amax for NVFP4 rowwise (and NVFP4 columnwise without
         // RHT), Hadamard-domain amax for NVFP4 columnwise with RHT
         float* plain_row = row_fmt == NVQ_FMT_NVFP4 ? row->amax : nullptr;
@@ -269,14 +269,20 @@ nvq_status quantize_impl(const void* x, int64_t M, int64_t K, int64_t ld, const 
     return cuda_status(launch_quantize(a, (int)row_fmt, (int)col_fmt, rht, sr != nullptr, row_tiles, stream));
 }
 
-// Test hook for the bounded waits: with NVQ_DEBUG_DROP_TMA=1 in the environment
-// (read at every GEMM call) the single-CTA GEMM kernel arms its first pipeline
-// stage but issues no copy into it, so every wait on that stage runs out, the
-// kernel records NVQ_ERR_TIMEOUT and returns.  Nothing faults or hangs.
-bool debug_drop_first_load()
+// Test hook for the bounded waits: with NVQ_DEBUG_DROP_TMA=1 in the
+// environment (read once per process), the first GEMM the process launches
+// arms its first pipeline stage but issues no copy into it, so every wait on
+// that stage runs out, the kernel records NVQ_ERR_TIMEOUT and returns (the
+// CTA-pair kernel stops both CTAs of a pair); later launches are normal.
+// Nothing faults or hangs.
+bool debug_drop_this_launch()
 {
-    const char* e = std::getenv("NVQ_DEBUG_DROP_TMA");
-    return e && e[0] == '1';
+    static const bool on = [] {
+        const char* e = std::getenv("NVQ_DEBUG_DROP_TMA");
+        return e && e[0] == '1';
+    }();
+    static std::atomic<bool> used{false};
+    return on && !used.exchange(true);
 }
 
 nvq_status gemm_prepare(const nvq_qtensor* A, const nvq_qtensor* B, int64_t n_out, CUtensorMap* am, CUtensorMap* bm,
@@ -306,7 +312,7 @@ nvq_status gemm_prepare(const nvq_qtensor* A, const nvq_qtensor* B, int64_t n_ou
     g->block_n = gemm_block_n(n_out);
     int* status = nullptr;
     if (device_setup(&status) != cudaSuccess) return NVQ_ERR_CUDA;
-    g->use_pair = (g->block_n == 256 && pair_gemm_enabled() && device_pair_ok() && !debug_drop_first_load()) ? 1 : 0;
+    g->use_pair = (g->block_n == 256 && pair_gemm_enabled() && device_pair_ok()) ? 1 : 0;
     g->any_k = (A->rows > 0 && A->cols > 0 && B->rows > 0 && B->cols > 0) ? 1 : 0;
     const int64_t eb = f == NVQ_FMT_NVFP4 ? 2 : 1;  // elements per byte
     // the pair kernel loads 128 rows of B per CTA; the single-CTA one block_n rows
@@ -347,7 +353,7 @@ nvq_status gemm_launch(const CUtensorMap& am, const CUtensorMap& bm, GemmArgs& g
     int num_sms = 0;
     if (device_setup(&status, &num_sms) != cudaSuccess) return NVQ_ERR_CUDA;
     g.status = status;
-    g.debug_drop_first_load = debug_drop_first_load() ? 1 : 0;
+    g.debug_drop_first_load = debug_drop_this_launch() ? 1 : 0;
     // pair tiles: each group's 128-row tiles taken two at a time
     int pm = 0;
     for (int i = 0; i < g.G; ++i) {
@@ -374,6 +380,51 @@ nvq_status gemm_launch(const CUtensorMap& am, const CUtensorMap& bm, GemmArgs& g
         g.c_tma = 1;
     if (g.use_pair) return cuda_status(launch_gemm_pair(&am, &bm, &cm, g, num_sms, stream));
     return cuda_status(launch_gemm(&am, &bm, g, num_sms, stream));
+}
+
+// nvq_gemm_tn with the optional output amaxes.
+nvq_status gemm_tn_impl(const nvq_qtensor* A, const nvq_qtensor* B, const void* bias, void* C, int64_t ldc,
+                        int c_fp32, const nvq_rht* rht, float* c_amax, float* c_amax_rht, cudaStream_t stream)
+{
+    if (!A || !B) return NVQ_ERR_NULL;
+    if (A->fmt == B->fmt && A->cols != B->cols) return NVQ_ERR_SHAPE;
+    if ((c_amax && (reinterpret_cast<uintptr_t>(c_amax) & 3)) || (c_amax_rht && (reinterpret_cast<uintptr_t>(c_amax_rht) & 3)))
+        return NVQ_ERR_ALIGN;
+    uint32_t mask = 0;
+    if (c_amax_rht) {
+        bool ok;
+        mask = sign_mask(rht, &ok);
+        if (!ok) return NVQ_ERR_SHAPE;
+    }
+    CUtensorMap am, bm;
+    GemmArgs* g = new (std::nothrow) GemmArgs;
+    if (!g) return NVQ_ERR_CUDA;
+    nvq_status s = gemm_prepare(A, B, B->rows, &am, &bm, g);
+    if (s == NVQ_OK) s = check_c(C, ldc, B->rows, c_fp32);
+    if (s == NVQ_OK && bias && !aligned16(bias)) s = NVQ_ERR_ALIGN;
+    if (s == NVQ_OK && c_amax && cudaMemsetAsync(c_amax, 0, sizeof(float), stream) != cudaSuccess) s = NVQ_ERR_CUDA;
+    if (s == NVQ_OK && c_amax_rht && cudaMemsetAsync(c_amax_rht, 0, sizeof(float), stream) != cudaSuccess)
+        s = NVQ_ERR_CUDA;
+    if (s == NVQ_OK) {
+        g->c_amax = c_amax;
+        g->c_amax_rht = c_amax_rht;
+        g->rht_sign_mask = mask;
+        g->n_tiles = (int)(B->rows / g->block_n);
+        g->total_m_tiles = (int)(A->rows / 128);
+        g->G = 1;
+        g->bias = static_cast<const uint16_t*>(bias);
+        g->C = C;
+        g->ldc = ldc;
+        g->c_fp32 = c_fp32 ? 1 : 0;
+        GemmGroup& gr = g->groups[0];
+        gr.m_tile0 = 0;
+        gr.m_tiles = g->total_m_tiles;
+        gr.k_len = (int32_t)A->cols;
+        gr.rows_valid = (int32_t)A->rows;
+        s = gemm_launch(am, bm, *g, B->rows, stream);
+    }
+    delete g;
+    return s;
 }
 
 }  // namespace
@@ -462,63 +513,79 @@ nvq_status nvq_hybrid_quantize(const void* x, int64_t M, int64_t K, int64_t ld, 
 nvq_status nvq_gemm_tn(const nvq_qtensor* A, const nvq_qtensor* B, const void* bias, void* C, int64_t ldc,
                        int c_fp32, nvq_stream stream)
 {
-    if (!A || !B) return NVQ_ERR_NULL;
-    if (A->fmt == B->fmt && A->cols != B->cols) return NVQ_ERR_SHAPE;
-    CUtensorMap am, bm;
-    GemmArgs* g = new (std::nothrow) GemmArgs;
-    if (!g) return NVQ_ERR_CUDA;
-    nvq_status s = gemm_prepare(A, B, B->rows, &am, &bm, g);
-    if (s == NVQ_OK) s = check_c(C, ldc, B->rows, c_fp32);
-    if (s == NVQ_OK && bias && !aligned16(bias)) s = NVQ_ERR_ALIGN;
-    if (s == NVQ_OK) {
-        g->n_tiles = (int)(B->rows / g->block_n);
-        g->total_m_tiles = (int)(A->rows / 128);
-        g->G = 1;
-        g->bias = static_cast<const uint16_t*>(bias);
-        g->C = C;
-        g->ldc = ldc;
-        g->c_fp32 = c_fp32 ? 1 : 0;
-        GemmGroup& gr = g->groups[0];
-        gr.m_tile0 = 0;
-        gr.m_tiles = g->total_m_tiles;
-        gr.k_len = (int32_t)A->cols;
-        gr.rows_valid = (int32_t)A->rows;
-        s = gemm_launch(am, bm, *g, B->rows, reinterpret_cast<cudaStream_t>(stream));
-    }
-    delete g;
-    return s;
+    return gemm_tn_impl(A, B, bias, C, ldc, c_fp32, nullptr, nullptr, nullptr, reinterpret_cast<cudaStream_t>(stream));
+}
+
+nvq_status nvq_gemm_tn_amax(const nvq_qtensor* A, const nvq_qtensor* B, const void* bias, void* C, int64_t ldc,
+                            int c_fp32, const nvq_rht* rht, float* c_amax, float* c_amax_rht, nvq_stream stream)
+{
+    if (c_amax_rht && !rht) return NVQ_ERR_NULL;
+    return gemm_tn_impl(A, B, bias, C, ldc, c_fp32, rht, c_amax, c_amax_rht, reinterpret_cast<cudaStream_t>(stream));
+}
+
+nvq_status nvq_nvfp4_quantize_ex(const void* x, int64_t M, int64_t K, int64_t ld, int dirs, const nvq_rht* rht_col,
+                                 const nvq_sr* sr, int flags, nvq_qtensor* row, nvq_qtensor* col, nvq_stream stream)
+{
+    if (dirs & ~(NVQ_DIR_ROW | NVQ_DIR_COL)) return NVQ_ERR_UNSUPPORTED;
+    if (flags & ~NVQ_AMAX_GIVEN) return NVQ_ERR_UNSUPPORTED;
+    return quantize_impl(x, M, K, ld, nullptr, 1, (dirs & NVQ_DIR_ROW) ? NVQ_FMT_NVFP4 : NVQ_FMT_NONE,
+                         (dirs & NVQ_DIR_COL) ? NVQ_FMT_NVFP4 : NVQ_FMT_NONE, rht_col, sr, row, col,
+                         reinterpret_cast<cudaStream_t>(stream), (flags & NVQ_AMAX_GIVEN) != 0);
+}
+nvq_status nvq_nvfp4_linear_fwd_ex(const void* x, const void* w, const void* bias, int64_t M, int64_t N, int64_t K,
+                                   const nvq_rht* rht, int flags, void* y, float* y_amax, float* y_amax_rht,
+                                   nvq_qtensor* x_row, nvq_qtensor* w_row, nvq_qtensor* saved_x_col,
+                                   nvq_qtensor* saved_w_col, nvq_stream stream)
+{
+    if (!x || !w || !y || !x_row || !w_row) return NVQ_ERR_NULL;
+    if (M % 128 || N % 128 || K % 128 || M <= 0 || N <= 0 || K <= 0) return NVQ_ERR_SHAPE;
+    if (flags & ~NVQ_AMAX_GIVEN) return NVQ_ERR_UNSUPPORTED;
+    if (y_amax_rht && !rht) return NVQ_ERR_NULL;
+    const bool xc = saved_x_col && saved_x_col->data, wc = saved_w_col && saved_w_col->data;
+    nvq_status s = nvq_nvfp4_quantize_ex(x, M, K, K, NVQ_DIR_ROW | (xc ? NVQ_DIR_COL : 0), rht, nullptr, flags, x_row,
+                                         xc ? saved_x_col : nullptr, stream);
+    if (s != NVQ_OK) return s;
+    s = nvq_nvfp4_quantize(w, N, K, K, NVQ_DIR_ROW | (wc ? NVQ_DIR_COL : 0), nullptr, nullptr, w_row,
+                           wc ? saved_w_col : nullptr, stream);
+    if (s != NVQ_OK) return s;
+    return nvq_gemm_tn_amax(x_row, w_row, bias, y, N, 0, rht, y_amax, y_amax_rht, stream);
 }
 
 nvq_status nvq_nvfp4_linear_fwd(const void* x, const void* w, const void* bias, int64_t M, int64_t N, int64_t K,
                                 const nvq_rht* rht, void* y, nvq_qtensor* x_row, nvq_qtensor* w_row,
                                 nvq_qtensor* saved_x_col, nvq_qtensor* saved_w_col, nvq_stream stream)
 {
-    if (!x || !w || !y || !x_row || !w_row) return NVQ_ERR_NULL;
-    if (M % 128 || N % 128 || K % 128 || M <= 0 || N <= 0 || K <= 0) return NVQ_ERR_SHAPE;
-    const bool xc = saved_x_col && saved_x_col->data, wc = saved_w_col && saved_w_col->data;
-    nvq_status s = nvq_nvfp4_quantize(x, M, K, K, NVQ_DIR_ROW | (xc ? NVQ_DIR_COL : 0), rht, nullptr, x_row,
-                                      xc ? saved_x_col : nullptr, stream);
-    if (s != NVQ_OK) return s;
-    s = nvq_nvfp4_quantize(w, N, K, K, NVQ_DIR_ROW | (wc ? NVQ_DIR_COL : 0), nullptr, nullptr, w_row,
-                           wc ? saved_w_col : nullptr, stream);
-    if (s != NVQ_OK) return s;
-    return nvq_gemm_tn(x_row, w_row, bias, y, N, 0, stream);
+    return nvq_nvfp4_linear_fwd_ex(x, w, bias, M, N, K, rht, 0, y, nullptr, nullptr, x_row, w_row, saved_x_col,
+                                   saved_w_col, stream);
+}
+
+nvq_status nvq_nvfp4_linear_bwd_quantize_ex(const void* dy, int64_t M, int64_t N, const nvq_rht* rht,
+                                            const nvq_sr* sr, int flags, nvq_qtensor* dy_row, nvq_qtensor* dy_col,
+                                            nvq_stream stream)
+{
+    if (M % 128 || N % 128) return NVQ_ERR_SHAPE;
+    return nvq_nvfp4_quantize_ex(dy, M, N, N, NVQ_DIR_ROW | NVQ_DIR_COL, rht, sr, flags, dy_row, dy_col, stream);
 }
 
 nvq_status nvq_nvfp4_linear_bwd_quantize(const void* dy, int64_t M, int64_t N, const nvq_rht* rht,
                                          const nvq_sr* sr, nvq_qtensor* dy_row, nvq_qtensor* dy_col,
                                          nvq_stream stream)
 {
-    if (M % 128 || N % 128) return NVQ_ERR_SHAPE;
-    return nvq_nvfp4_quantize(dy, M, N, N, NVQ_DIR_ROW | NVQ_DIR_COL, rht, sr, dy_row, dy_col, stream);
+    return nvq_nvfp4_linear_bwd_quantize_ex(dy, M, N, rht, sr, 0, dy_row, dy_col, stream);
+}
+
+nvq_status nvq_nvfp4_linear_dgrad_ex(const nvq_qtensor* dy_row, const nvq_qtensor* saved_w_col, const nvq_rht* rht,
+                                     void* dx, float* dx_amax, float* dx_amax_rht, nvq_stream stream)
+{
+    if (!dy_row || !saved_w_col) return NVQ_ERR_NULL;
+    if (dy_row->fmt != NVQ_FMT_NVFP4 || saved_w_col->fmt != NVQ_FMT_NVFP4) return NVQ_ERR_UNSUPPORTED;
+    return nvq_gemm_tn_amax(dy_row, saved_w_col, nullptr, dx, saved_w_col->rows, 0, rht, dx_amax, dx_amax_rht, stream);
 }
 
 nvq_status nvq_nvfp4_linear_dgrad(const nvq_qtensor* dy_row, const nvq_qtensor* saved_w_col, void* dx,
                                   nvq_stream stream)
 {
-    if (!dy_row || !saved_w_col) return NVQ_ERR_NULL;
-    if (dy_row->fmt != NVQ_FMT_NVFP4 || saved_w_col->fmt != NVQ_FMT_NVFP4) return NVQ_ERR_UNSUPPORTED;
-    return nvq_gemm_tn(dy_row, saved_w_col, nullptr, dx, saved_w_col->rows, 0, stream);
+    return nvq_nvfp4_linear_dgrad_ex(dy_row, saved_w_col, nullptr, dx, nullptr, nullptr, stream);
 }
 
 nvq_status nvq_nvfp4_linear_wgrad(const nvq_qtensor* dy_col, const nvq_qtensor* saved_x_col, void* dw,
@@ -724,6 +791,13 @@ nvq_status nvq_get_device_status(nvq_stream stream, int32_t* code)
     return NVQ_OK;
 }
 
-const char* nvq_version(void) { return "nvq 0.1 (sm_103a)"; }
+int nvq_gemm_pair_available(void)
+{
+    int* status = nullptr;
+    if (device_setup(&status) != cudaSuccess) return -1;
+    return (pair_gemm_enabled() && device_pair_ok()) ? 1 : 0;
+}
+
+const char* nvq_version(void) { return "nvq 0.2 (sm_103a)"; }
 
 }  // extern "C"

@@ -372,6 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int quad = warp & 3;
         const int half = (warp - kFirstEpiWarp) >> 2;
         const int r = quad * 32 + lane;     // tile row = TMEM lane
+        EpiAmax am = epi_amax_init(args, lane);
         uint32_t tl_i = 0;
         for (int t = blockIdx.x; t < total; t += gridDim.x, ++tl_i) {
             const Tile tl = decode<BN, C::kStageK>(args, t);
@@ -394,12 +395,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int col0 = tl.n_tile * BN + half * kCols;
             const int64_t rowoff = gr.c_off + (int64_t)out_row * args.ldc + col0;
             const uint32_t taddr = tmem_base + (uint32_t)(as * BN + half * kCols) + ((uint32_t)(quad * 32) << 16);
-            epilogue_slice<kCols>(args, taddr, tl.num_kb > 0, alpha, col0, rowoff, row_ok, [&] {
+            epilogue_slice<kCols>(args, taddr, tl.num_kb > 0, alpha, col0, rowoff, row_ok, am, [&] {
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&acc_empty[as]);
             });
         }
+        epi_amax_publish(args, am, lane);
     }
 
     tc_fence_before();

@@ -59,6 +59,7 @@ constexpr int kRegsLow = 80;
 constexpr int kRegsHigh = 176;
 static_assert(8 * 32 * kRegsLow + 8 * 32 * kRegsHigh == kThreads * 128, "register split");
 constexpr uint32_t kTmemCols = 512;
+constexpr uint64_t kAbortGraceNs = 1000000;  // 1 ms
 
 // Each CTA's TMEM holds the B scales of all 256 columns (both halves of B):
 // the pair MMA reads the full B scale set from each CTA's TMEM (holding only
@@ -140,6 +141,8 @@ __device__ __forceinline__ PairTile decode(const GemmArgs& a, int t, uint32_t ra
     return r;
 }
 
+// Bounded wait that gives up when this CTA has aborted; a wait that runs out
+// raises the abort flags of both CTAs of the pair.
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, int* status, volatile int* abort_flag)
 {
     if (mbar_try_wait(bar, parity)) return true;
@@ -151,6 +154,7 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, in
             if (globaltimer_ns() - t0 > kWaitLimitNs) {
                 record_error(status, kErrTimeout);
                 *abort_flag = 1;
+                set_partner_abort(abort_flag);
                 return false;
             }
         }
@@ -222,6 +226,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int quad = warp & 3;
         const int half = (warp - kFirstEpiWarp) >> 2;
         const int r = quad * 32 + lane;
+        EpiAmax am = epi_amax_init(args, lane);
         uint32_t tl_i = 0;
         for (int t = pair; t < total; t += n_pairs, ++tl_i) {
             const PairTile tl = decode<C::kStageK>(args, t, rank);
@@ -250,10 +255,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             if (args.c_tma && tl.mt_local * BM + BM <= gr.rows_valid)
                 epilogue_slice_tma<kCols>(args, &c_map, smem + C::kEpi + (warp - kFirstEpiWarp) * 4096, taddr,
                                           tl.num_kb > 0, alpha, col0, gr.c_row0 + tl.mt_local * BM + quad * 32, lane,
-                                          release);
+                                          am, release);
             else
-                epilogue_slice<kCols>(args, taddr, tl.num_kb > 0, alpha, col0, rowoff, row_ok, release);
+                epilogue_slice<kCols>(args, taddr, tl.num_kb > 0, alpha, col0, rowoff, row_ok, am, release);
         }
+        epi_amax_publish(args, am, lane);
         if (lane == 0) bulk_wait_group0();  // this warp's C stores completed before the CTA exits
     } else {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
@@ -268,11 +274,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     const PairTile tl = decode<C::kStageK>(args, t, rank);
                     for (int kb = 0; kb < tl.num_kb; ++kb, ++it) {
                         const int s = it % C::kStages;
-                        mbar_wait_flag(&empty[s], ((it / C::kStages) & 1) ^ 1, abort_flag);
-                        const uint32_t live = live_flag(abort_flag);
+                        mbar_wait_flag_pair(&empty[s], ((it / C::kStages) & 1) ^ 1, abort_flag);
+                        uint32_t live = live_flag(abort_flag);
+                        // test hook: the leader arms the first stage, neither CTA loads into it
+                        const uint32_t arm = live & leader;
+                        live = (args.debug_drop_first_load && it == 0) ? 0u : live;
                         const int ka = tl.a_k0 + kb * C::kStageK, kbb = tl.b_k0 + kb * C::kStageK;
-                        mbar_arrive_expect_tx_if(&full[s], 4u * kHalfTileBytes, live & leader);  // A + B of both CTAs
-                        n_armed += live;
+                        mbar_arrive_expect_tx_if(&full[s], 4u * kHalfTileBytes, arm);  // A + B of both CTAs
+                        n_armed += arm;
                         const uint32_t bar = map_to_rank(&full[s], 0);
                         const int b_row = tl.b_row_pair + (int)rank * 128;
                         tma_load_2d_pair_if(smem + C::kA + s * kHalfTileBytes, &a_map, bar, FMT == 1 ? ka / 2 : ka, tl.a_row, live);
@@ -299,10 +308,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 uint32_t sfa_col = tmem_base + C::kSfCol0;
                 for (int t = pair; t < total; t += n_pairs, ++tl_i) {
                     const PairTile tl = decode<C::kStageK>(args, t, 0);
-                    mbar_wait_flag(acc_empty, (tl_i & 1) ^ 1, abort_flag);
+                    mbar_wait_flag_pair(acc_empty, (tl_i & 1) ^ 1, abort_flag);
                     tc_fence_after();
                     for (int kb = 0; kb < tl.num_kb; ++kb) {
-                        live = mbar_wait_live(&full[s], par, abort_flag);  // A/B bytes and scales
+                        live = mbar_wait_live_pair(&full[s], par, abort_flag);  // A/B bytes and scales
                         tc_fence_after();
                         const int n_mma = min(C::kStageK, tl.k_len - kb * C::kStageK) / C::kMmaK;
                         const uint32_t sfb_col = sfa_col + C::kSfaCols;
@@ -341,7 +350,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 for (int kb = 0; kb < tl.num_kb; ++kb, ++it) {
                     const int s = it % C::kStages;
                     int good = 1;
-                    if (lane == 0) good = wait_or_abort(&sf_full[s], (it / C::kStages) & 1, args.status, abort_flag);
+                    if (lane == 0)
+                        good = wait_or_abort(&sf_full[s], (it / C::kStages) & 1, args.status, abort_flag);
                     good = __shfl_sync(0xFFFFFFFFu, good, 0);
                     if (!good) {
                         ok = false;
@@ -381,7 +391,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     const PairTile tl = decode<C::kStageK>(args, t, rank);
                     for (int kb = 0; kb < tl.num_kb; ++kb, ++it) {
                         const int s = it % C::kStages;
-                        mbar_wait_flag(&empty[s], ((it / C::kStages) & 1) ^ 1, abort_flag);
+                        mbar_wait_flag_pair(&empty[s], ((it / C::kStages) & 1) ^ 1, abort_flag);
                         const uint32_t live = live_flag(abort_flag);
                         const int ka = tl.a_k0 + kb * C::kStageK, kbb = tl.b_k0 + kb * C::kStageK;
                         const int left = tl.k_len - kb * C::kStageK;
@@ -410,6 +420,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
     }  // warpgroups 0-1
 
+    // After an abort, copies this CTA issued into stages the leader never
+    // armed complete on no barrier anyone waits for: give them a bounded
+    // grace period (a copy lands within microseconds) before the CTA can exit.
+    if (threadIdx.x == 0 && *abort_flag) grace_wait_ns(kAbortGraceNs);
     tc_fence_before();
     __syncthreads();
     cluster_sync();  // the partner no longer issues MMAs, copies or arrivals that reach this CTA

@@ -10,6 +10,85 @@
 
 namespace nvq {
 
+// Optional amaxes of the stored output, for the quantizer of the next
+// operation (so it can skip its own amax pass).  Each epilogue warp keeps
+// running maxima across its tiles and publishes them once, at the end of the
+// kernel (one atomic per warp instead of one per tile).
+//   plain: max |C| over the stored values (after rounding to the output type);
+//   rht:   max |H16 (s .* u)| over the 16-row column blocks u of C, before the
+//          1/4 of the transform (applied once to the maximum: rounding is
+//          monotonic).  A lane holds one row, so the 16 rows of a block are 16
+//          consecutive lanes and the fp32 butterfly runs across them: stage h
+//          pairs lanes i and i ^ h, the lane with bit h clear keeps a + b and
+//          the other a - b, in the order the columnwise quantizer applies
+//          (spans 1, 2, 4, 8).
+struct EpiAmax {
+    float plain;
+    float rht;
+    uint32_t flip;       // sign bit to apply to this lane's row (sign[lane & 15] == -1)
+    uint32_t neg[4];     // sign bit of the own value in stage h = 1, 2, 4, 8
+    bool on_plain, on_rht;
+};
+
+__device__ __forceinline__ EpiAmax epi_amax_init(const GemmArgs& args, int lane)
+{
+    EpiAmax am;
+    am.plain = 0.0f;
+    am.rht = 0.0f;
+    am.flip = ((args.rht_sign_mask >> (lane & 15)) & 1u) << 31;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) am.neg[b] = (lane & (1 << b)) ? 0x80000000u : 0u;
+    am.on_plain = args.c_amax != nullptr;
+    am.on_rht = args.c_amax_rht != nullptr;
+    return am;
+}
+
+__device__ __forceinline__ void epi_amax_add(EpiAmax& am, float v)
+{
+    am.plain = fmaxf(am.plain, fabsf(v));
+    if (am.on_rht) {  // warp-uniform
+        float u = __uint_as_float(__float_as_uint(v) ^ am.flip);
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            const float p = __shfl_xor_sync(0xFFFFFFFFu, u, 1 << b);
+            u = __fadd_rn(p, __uint_as_float(__float_as_uint(u) ^ am.neg[b]));
+        }
+        am.rht = fmaxf(am.rht, fabsf(u));
+    }
+}
+
+// n packed bf16 pairs (the stored values)
+template <int n>
+__device__ __forceinline__ void epi_amax_add_bf16(EpiAmax& am, const uint32_t* w)
+{
+    if (!am.on_plain && !am.on_rht) return;
+#pragma unroll
+    for (int i = 0; i < n; ++i) {
+        epi_amax_add(am, __uint_as_float(w[i] << 16));
+        epi_amax_add(am, __uint_as_float(w[i] & 0xFFFF0000u));
+    }
+}
+
+__device__ __forceinline__ float epi_warp_max(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    return v;
+}
+
+// Publishes the warp's maxima (non-negative floats order like their bits).
+__device__ __forceinline__ void epi_amax_publish(const GemmArgs& args, EpiAmax& am, int lane)
+{
+    if (am.on_plain) {
+        const float m = epi_warp_max(am.plain);
+        if (lane == 0) atomicMax(reinterpret_cast<unsigned int*>(args.c_amax), __float_as_uint(m));
+    }
+    if (am.on_rht) {
+        const float m = __fmul_rn(epi_warp_max(am.rht), 0.25f);
+        if (lane == 0) atomicMax(reinterpret_cast<unsigned int*>(args.c_amax_rht), __float_as_uint(m));
+    }
+}
+
 // 32 accumulator columns (fp32 bits) -> alpha * acc (+ bias) as 16 bf16 pairs
 // (column 2i in the low half of out[i]); bcol: C column of v[0].
 __device__ __forceinline__ void pack32_bf16(const GemmArgs& args, const uint32_t (&v)[32], float alpha, int bcol,
@@ -61,7 +140,7 @@ __device__ __forceinline__ void pack_slice_bf16(const GemmArgs& args, uint32_t t
 // completed.
 template <int kCols, typename Release>
 __device__ __forceinline__ void epilogue_slice(const GemmArgs& args, uint32_t taddr, bool have_k, float alpha,
-                                               int col0, int64_t rowoff, bool row_ok, Release release)
+                                               int col0, int64_t rowoff, bool row_ok, EpiAmax& am, Release release)
 {
     static_assert(kCols % 64 == 0, "64-column granularity");
     if (!args.c_fp32) {
@@ -70,6 +149,7 @@ __device__ __forceinline__ void epilogue_slice(const GemmArgs& args, uint32_t ta
         uint32_t packed[kCols / 2];
         pack_slice_bf16<kCols>(args, taddr, have_k, alpha, col0, packed);
         release();
+        epi_amax_add_bf16<kCols / 2>(am, packed);
         if (!row_ok) return;
         if (args.c_st32) {  // 32-byte stores, one full L2 sector each
             uint16_t* dst = reinterpret_cast<uint16_t*>(args.C) + rowoff;
@@ -98,7 +178,7 @@ __device__ __forceinline__ void epilogue_slice(const GemmArgs& args, uint32_t ta
             for (int i = 0; i < 64; ++i) v[i] = 0u;
         }
         if (p == kCols / 64 - 1) release();
-        if (!row_ok) continue;
+        if (!row_ok && !am.on_plain && !am.on_rht) continue;
         float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(args.C) + rowoff + p * 64);
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
@@ -108,8 +188,9 @@ __device__ __forceinline__ void epilogue_slice(const GemmArgs& args, uint32_t ta
                 float y = __fmul_rn(alpha, __uint_as_float(v[4 * i + e]));
                 if (args.bias) y = __fadd_rn(y, __uint_as_float((uint32_t)args.bias[col0 + p * 64 + 4 * i + e] << 16));
                 f[e] = y;
+                if (am.on_plain || am.on_rht) epi_amax_add(am, y);
             }
-            dst[i] = make_float4(f[0], f[1], f[2], f[3]);
+            if (row_ok) dst[i] = make_float4(f[0], f[1], f[2], f[3]);
         }
     }
 }
@@ -129,7 +210,7 @@ __device__ __forceinline__ void epilogue_slice(const GemmArgs& args, uint32_t ta
 template <int kCols, typename Release>
 __device__ __forceinline__ void epilogue_slice_tma(const GemmArgs& args, const CUtensorMap* c_map, uint8_t* stage,
                                                    uint32_t taddr, bool have_k, float alpha, int col0, int c_row0,
-                                                   int lane, Release release)
+                                                   int lane, EpiAmax& am, Release release)
 {
     static_assert(kCols == 128, "four 32-column chunks");
     uint8_t* row = stage + lane * 128;
@@ -152,6 +233,7 @@ __device__ __forceinline__ void epilogue_slice_tma(const GemmArgs& args, const C
         uint32_t packed[32];
         pack32_bf16(args, v[2 * b], alpha, col0 + 64 * b, &packed[0]);
         pack32_bf16(args, v[2 * b + 1], alpha, col0 + 64 * b + 32, &packed[16]);
+        epi_amax_add_bf16<32>(am, packed);
         if (lane == 0) bulk_wait_group_read0();  // the previous store has read the buffer
         __syncwarp();
 #pragma unroll

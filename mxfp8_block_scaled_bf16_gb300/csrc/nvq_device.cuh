@@ -151,6 +151,92 @@ __device__ __forceinline__ uint32_t mbar_wait_live(uint64_t* bar, uint32_t parit
     return live;
 }
 
+// CTA-pair forms of the two waits above: a wait that runs out also raises the
+// partner CTA's abort flag (the same shared-memory offset in CTA rank ^ 1 of
+// the cluster, mapped only on that path so it costs no register), so both
+// CTAs of the pair stop issuing copies and tensor-core work together instead
+// of the partner finding out only when its own waits run out.
+__device__ __forceinline__ void mbar_wait_flag_pair(uint64_t* bar, uint32_t parity, volatile int* abort_flag)
+{
+    asm volatile(
+        "{\n\t.reg .pred P1;\n\t.reg .b64 t0, t1;\n\t.reg .b32 ab, pr, pa;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 P1, [%0], %1;\n\t"
+        "@P1 bra.uni DONE;\n\t"
+        "mov.u64 t0, %%globaltimer;\n\t"
+        "LOOP:\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 P1, [%0], %1;\n\t"
+        "@P1 bra.uni DONE;\n\t"
+        "ld.volatile.shared.u32 ab, [%2];\n\t"
+        "setp.ne.u32 P1, ab, 0;\n\t"
+        "@P1 bra.uni DONE;\n\t"
+        "mov.u64 t1, %%globaltimer;\n\t"
+        "sub.u64 t1, t1, t0;\n\t"
+        "setp.lt.u64 P1, t1, %3;\n\t"
+        "@P1 bra.uni LOOP;\n\t"
+        "st.volatile.shared.u32 [%2], 1;\n\t"
+        "mov.u32 pr, %%cluster_ctarank;\n\t"
+        "xor.b32 pr, pr, 1;\n\t"
+        "mapa.shared::cluster.u32 pa, %2, pr;\n\t"
+        "st.relaxed.cluster.shared::cluster.u32 [pa], 1;\n\t"
+        "DONE:\n\t}" ::"r"(smem_u32(bar)),
+        "r"(parity), "r"(smem_u32(const_cast<int*>(abort_flag))), "l"(kWaitLimitNs)
+        : "memory");
+}
+
+__device__ __forceinline__ uint32_t mbar_wait_live_pair(uint64_t* bar, uint32_t parity, volatile int* abort_flag)
+{
+    uint32_t live;
+    asm volatile(
+        "{\n\t.reg .pred P1;\n\t.reg .b64 t0, t1;\n\t.reg .b32 ab, pr, pa;\n\t"
+        "mov.u32 %0, 1;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 P1, [%1], %2;\n\t"
+        "@P1 bra.uni DONE;\n\t"
+        "mov.u64 t0, %%globaltimer;\n\t"
+        "LOOP:\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 P1, [%1], %2;\n\t"
+        "@P1 bra.uni DONE;\n\t"
+        "ld.volatile.shared.u32 ab, [%3];\n\t"
+        "setp.ne.u32 P1, ab, 0;\n\t"
+        "@P1 bra.uni GAVEUP;\n\t"
+        "mov.u64 t1, %%globaltimer;\n\t"
+        "sub.u64 t1, t1, t0;\n\t"
+        "setp.lt.u64 P1, t1, %4;\n\t"
+        "@P1 bra.uni LOOP;\n\t"
+        "st.volatile.shared.u32 [%3], 1;\n\t"
+        "mov.u32 pr, %%cluster_ctarank;\n\t"
+        "xor.b32 pr, pr, 1;\n\t"
+        "mapa.shared::cluster.u32 pa, %3, pr;\n\t"
+        "st.relaxed.cluster.shared::cluster.u32 [pa], 1;\n\t"
+        "GAVEUP:\n\t"
+        "mov.u32 %0, 0;\n\t"
+        "DONE:\n\t}"
+        : "=r"(live)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(smem_u32(const_cast<int*>(abort_flag))), "l"(kWaitLimitNs)
+        : "memory");
+    return live;
+}
+
+// Raises the partner CTA's abort flag (the flag at the same offset in CTA
+// rank ^ 1 of the cluster).
+__device__ __forceinline__ void set_partner_abort(volatile int* abort_flag)
+{
+    asm volatile(
+        "{\n\t.reg .b32 pr, pa;\n\t"
+        "mov.u32 pr, %%cluster_ctarank;\n\t"
+        "xor.b32 pr, pr, 1;\n\t"
+        "mapa.shared::cluster.u32 pa, %0, pr;\n\t"
+        "st.relaxed.cluster.shared::cluster.u32 [pa], 1;\n\t}" ::"r"(smem_u32(const_cast<int*>(abort_flag)))
+        : "memory");
+}
+
+// Spins for `ns` nanoseconds of %globaltimer (bounded by construction).
+__device__ __forceinline__ void grace_wait_ns(uint64_t ns)
+{
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < ns) {
+    }
+}
+
 // 1 while the CTA has not aborted (read after a mbar_wait_flag).
 __device__ __forceinline__ uint32_t live_flag(volatile int* abort_flag) { return *abort_flag == 0 ? 1u : 0u; }
 

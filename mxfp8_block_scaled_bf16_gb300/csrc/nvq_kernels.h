@@ -92,6 +92,12 @@ struct GemmArgs {
     int c_tma;   // bf16 C stored through the C tensor map (CTA-pair kernel)
     int* status;           // device status word
     int debug_drop_first_load;  // test hook: arm stage 0's barrier but issue no copy
+    // optional amax of the stored output (single-problem GEMMs): max |C|, and
+    // max |T(u)| over 16-row column blocks u of C (T: 16-point Hadamard
+    // transform with the sign vector below); zeroed by the caller
+    float* c_amax;
+    float* c_amax_rht;
+    uint32_t rht_sign_mask;  // bit i set: sign[i] == -1
     GemmGroup groups[kMaxGroups];
 };
 

@@ -96,3 +96,44 @@ def assert_gemm_close(got: torch.Tensor, ref64: np.ndarray, what: str, tol: floa
         frac = np.mean(ulps <= 1)
         assert frac >= 0.999, f"{what}: only {frac:.5f} of elements within 1 bf16 ulp"
     return rel
+
+
+def sample_positions(R, C, n, seed, line=None):
+    """n random (row, col) positions of an R x C output plus one row and one
+    column (the first `line` entries of each, all of them when line is None)."""
+    rng = np.random.default_rng(seed)
+    r = rng.integers(0, R, n)
+    c = rng.integers(0, C, n)
+    row = int(rng.integers(0, R))
+    col = int(rng.integers(0, C))
+    lc = C if line is None else min(C, line)
+    lr = R if line is None else min(R, line)
+    rows = np.concatenate([r, np.full(lc, row), np.arange(lr)])
+    cols = np.concatenate([c, np.arange(lc), np.full(lr, col)])
+    return rows, cols
+
+
+def check_sampled_gemm(got: torch.Tensor, fmt, a, b, K, rows, cols, what, tol=1e-3):
+    """got: bf16 GPU output (any device); a, b: oracle operands (codes, compact
+    scales, amax) of A [R][K] and B [C][K] in format fmt (1 NVFP4, 2 MXFP8).
+    The oracle computes each sampled output from its own operands in fp64; the
+    GPU values must be within relative Frobenius error tol of it rounded once to
+    bf16, and >= 99.9% of them within one bf16 ulp."""
+    ga = oracle.nvfp4_g(a[2]) if fmt == 1 else 1.0
+    gb = oracle.nvfp4_g(b[2]) if fmt == 1 else 1.0
+    ref = oracle.gemm_tn_sampled(fmt, a[0], a[1], ga, b[0], b[1], gb, K, rows, cols)
+    sel = got[torch.from_numpy(rows).to(got.device), torch.from_numpy(cols).to(got.device)].cpu()
+    g = sel.float().numpy().astype(np.float64)
+    refb = bf16_from_bits(oracle.to_bf16_rne(ref)).float().numpy().astype(np.float64)
+    nrm = np.linalg.norm(refb)
+    rel = np.linalg.norm(g - refb) / (nrm if nrm > 0 else 1.0)
+    assert rel <= tol, f"{what}: sampled relative Frobenius error {rel:.3e}"
+    gb_ = bits(sel).astype(np.int32)
+    rb = oracle.to_bf16_rne(ref).astype(np.int32)
+
+    def ordered(v):
+        return np.where(v & 0x8000, -(v & 0x7FFF), v & 0x7FFF)
+
+    frac = np.mean(np.abs(ordered(gb_) - ordered(rb)) <= 1)
+    assert frac >= 0.999, f"{what}: {frac:.5f} of sampled outputs within 1 bf16 ulp"
+    return rel

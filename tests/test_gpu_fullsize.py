@@ -20,7 +20,8 @@ import oracle
 import mxfp8_block_scaled_bf16_gb300 as nvq
 from mxfp8_block_scaled_bf16_gb300 import inputs
 
-from gpu_util import assert_codes_equal, assert_scales_equal, bits, bf16_from_bits, qt_codes, qt_scales
+from gpu_util import (assert_codes_equal, assert_scales_equal, bits, check_sampled_gemm, qt_codes, qt_scales,
+                      sample_positions)
 
 pytestmark = pytest.mark.gpu
 
@@ -33,34 +34,8 @@ def _lib():
     assert nvq.device_status() == 0
 
 
-def _sample_positions(R, C, n, seed):
-    rng = np.random.default_rng(seed)
-    r = rng.integers(0, R, n)
-    c = rng.integers(0, C, n)
-    row = int(rng.integers(0, R))
-    col = int(rng.integers(0, C))
-    rows = np.concatenate([r, np.full(C, row), np.arange(R)])
-    cols = np.concatenate([c, np.arange(C), np.full(R, col)])
-    return rows, cols
-
-
-def _check_sampled(got: torch.Tensor, fmt, a, b, K, rows, cols, what):
-    """a, b: oracle (codes, compact scales, amax) operands; got: bf16 GPU output."""
-    ga = oracle.nvfp4_g(a[2]) if fmt == 1 else 1.0
-    gb = oracle.nvfp4_g(b[2]) if fmt == 1 else 1.0
-    ref = oracle.gemm_tn_sampled(fmt, a[0], a[1], ga, b[0], b[1], gb, K, rows, cols)
-    g = got[torch.from_numpy(rows), torch.from_numpy(cols)].float().cpu().numpy().astype(np.float64)
-    refb = bf16_from_bits(oracle.to_bf16_rne(ref)).float().numpy().astype(np.float64)
-    rel = np.linalg.norm(g - refb) / np.linalg.norm(refb)
-    assert rel <= 1e-3, f"{what}: sampled relative Frobenius error {rel:.3e}"
-    gb_ = bits(got[torch.from_numpy(rows), torch.from_numpy(cols)]).astype(np.int32)
-    rb = oracle.to_bf16_rne(ref).astype(np.int32)
-
-    def ordered(v):
-        return np.where(v & 0x8000, -(v & 0x7FFF), v & 0x7FFF)
-
-    frac = np.mean(np.abs(ordered(gb_) - ordered(rb)) <= 1)
-    assert frac >= 0.999, f"{what}: {frac:.5f} of sampled outputs within 1 bf16 ulp"
+_sample_positions = sample_positions
+_check_sampled = check_sampled_gemm
 
 
 def test_llama3_8b_up_step_full_size():
@@ -110,31 +85,63 @@ def test_moe_grouped_full_size():
     picks = sorted(set([int(order[0]), int(order[1]), int(order[-1]), int(order[len(order) // 2]), 5, 40]))
     offs = np.concatenate([[0], np.cumsum(sizes)])
     poffs = np.concatenate([[0], np.cumsum([-(-m // 128) * 128 for m in sizes])])
+    P = int(poffs[-1])
     xb, wb, dyb = bits(x), bits(w), bits(dy)
-    xr_c, dyr_c = qt_codes(xr), qt_codes(dyr)
+    xr_c, dyr_c, wr_c = qt_codes(xr), qt_codes(dyr), qt_codes(wr)
+    xc_c, wc_c, dyc_c = qt_codes(xc), qt_codes(wc), qt_codes(dyc)
+    # columnwise MXFP8 scales in compact form (the columns of one expert are not
+    # whole scale tiles, so the swizzled buffers are read back whole)
+    xc_s = oracle.scale_unswizzle(qt_scales(xc), K, P // 32)
+    wc_s = oracle.scale_unswizzle(qt_scales(wc), K, G * Nn // 32)
+    dyc_s = oracle.scale_unswizzle(qt_scales(dyc), Nn, P // 32)
+
+    def rows_scales(q, r0, rows, compact, what):
+        """Swizzled scales of whole 128-row tiles [r0, r0 + rows) against the
+        oracle's compact scales (zero-padded to the tiles)."""
+        blk = 16 if q.fmt == nvq.NVFP4 else 32
+        nb = q.cols // blk
+        pad = np.zeros((rows, nb), np.uint8)
+        pad[:compact.shape[0]] = compact
+        want = oracle.scale_swizzle(pad)
+        t0 = (r0 // 128) * (-(-nb // 4)) * 512
+        got = qt_scales(q)[t0:t0 + want.size]
+        assert np.array_equal(got, want), what
+
     for g in picks:
         m, s0, p0 = sizes[g], int(offs[g]), int(poffs[g])
+        mp = -(-m // 128) * 128
+        # the expert's weights in both formats (every expert has N rows)
+        b = oracle.nvfp4_quantize_rows(wb[g])
+        assert_codes_equal(wr_c[g * Nn:(g + 1) * Nn], b[0], f"expert {g} w_row codes")
+        rows_scales(wr, g * Nn, Nn, b[1], f"expert {g} w_row scales")
+        db = oracle.mxfp8_quantize_cols(wb[g]) + (0.0,)
+        assert_codes_equal(wc_c[:, g * Nn:(g + 1) * Nn], db[0], f"expert {g} w_col codes")
+        assert np.array_equal(wc_s[:, g * Nn // 32:(g + 1) * Nn // 32], db[1]), f"expert {g} w_col scales"
         if m == 0:
             assert torch.count_nonzero(dw[g]).item() == 0
             continue
         # forward operands (NVFP4 rows) and output
         a = oracle.nvfp4_quantize_rows(xb[s0:s0 + m])
-        b = oracle.nvfp4_quantize_rows(wb[g])
         assert_codes_equal(xr_c[p0:p0 + m], a[0], f"expert {g} x_row codes")
+        assert not xr_c[p0 + m:p0 + mp].any(), f"expert {g} x_row pad rows"
+        rows_scales(xr, p0, mp, a[1], f"expert {g} x_row scales")
         assert xr.amax[g].item() == np.float32(a[2]) and wr.amax[g].item() == np.float32(b[2])
         rows, cols = _sample_positions(m, Nn, 512, 10 + g)
         _check_sampled(y[s0:s0 + m].cpu(), 1, a, b, K, rows, cols, f"expert {g} fwd")
         # dgrad: MXFP8 dy rows x MXFP8 W columns
         da = oracle.mxfp8_quantize_rows(dyb[s0:s0 + m]) + (0.0,)
-        db = oracle.mxfp8_quantize_cols(wb[g]) + (0.0,)
         assert_codes_equal(dyr_c[p0:p0 + m], da[0], f"expert {g} dy_row codes")
+        rows_scales(dyr, p0, mp, da[1], f"expert {g} dy_row scales")
         rows, cols = _sample_positions(m, K, 512, 20 + g)
         _check_sampled(dx[s0:s0 + m].cpu(), 2, da, db, Nn, rows, cols, f"expert {g} dgrad")
         # wgrad: MXFP8 columns over the expert's 128-padded tokens
-        mp = -(-m // 128) * 128
         xp = np.zeros((mp, K), np.uint16); xp[:m] = xb[s0:s0 + m]
         dp = np.zeros((mp, Nn), np.uint16); dp[:m] = dyb[s0:s0 + m]
         wa = oracle.mxfp8_quantize_cols(dp) + (0.0,)
         wbb = oracle.mxfp8_quantize_cols(xp) + (0.0,)
+        assert_codes_equal(dyc_c[:, p0:p0 + mp], wa[0], f"expert {g} dy_col codes")
+        assert np.array_equal(dyc_s[:, p0 // 32:(p0 + mp) // 32], wa[1]), f"expert {g} dy_col scales"
+        assert_codes_equal(xc_c[:, p0:p0 + mp], wbb[0], f"expert {g} x_col codes")
+        assert np.array_equal(xc_s[:, p0 // 32:(p0 + mp) // 32], wbb[1]), f"expert {g} x_col scales"
         rows, cols = _sample_positions(Nn, K, 512, 30 + g)
         _check_sampled(dw[g].cpu(), 2, wa, wbb, mp, rows, cols, f"expert {g} wgrad")

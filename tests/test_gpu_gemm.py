@@ -10,6 +10,8 @@ bit-exact fp32 output.
 
 Pages: "Add an NVFP4 quantization converter" (NVFP4 linear, Table 1 path;
 GEMM dims multiples of 128) and "Hybrid quantization" (MXFP8 GEMM)."""
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -91,6 +93,8 @@ def test_more_tiles_than_sm_pairs(fmt, K):
     (NVFP4) is 4.5 ring stages (a ragged last stage of 2 MMAs); K = 896 (MXFP8)
     is 7 stages, so the ring wraps inside each tile."""
     M, N = 2048, 2560
+    if os.environ.get("NVQ_GEMM_PAIR") != "0":
+        assert nvq.gemm_pair_available(), "output width 2560 should run on the CTA-pair kernel"
     a = _randn(M, K, seed=31)
     b = _randn(N, K, seed=32, std=0.05)
     if fmt == 1:

@@ -137,6 +137,22 @@ def test_edge_values():
             check_mxfp8_col(mc, t)
 
 
+def test_rht_overflow_is_what_the_header_says():
+    """Outside the stated domain: |x| close to FLT_MAX makes the fp32 butterfly
+    of the columnwise Hadamard transform overflow.  nvq.h says the call then
+    completes with no device error, the columnwise amax is +inf, and the
+    rowwise direction (no transform) is unaffected -- bit-exact here."""
+    vals = torch.tensor([3e38, 3e38, -3e38, 1.0, -2.5, 0.0, 448.0, 1e-30], dtype=torch.float32)
+    x = vals.repeat(64 * 64 // vals.numel())[: 64 * 64].reshape(64, 64).to(torch.bfloat16)
+    assert np.isinf(oracle.amax_rht_col(bits(x), SIGN))  # the transform does overflow
+    row, col = nvq.nvfp4_quantize(x.cuda(), 3, rht_sign=SIGN, sr=(5, 0))
+    torch.cuda.synchronize()
+    assert nvq.device_status() == 0
+    a = col.amax.item()
+    assert np.isinf(a) and a > 0
+    check_nvfp4_row(row, x, sr=(5, 0))
+
+
 def test_amax_entry_point():
     x = inputs.student_t3_outliers(512, 256)
     a, r = nvq.amax(x.cuda(), rht_sign=SIGN)
