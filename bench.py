@@ -654,9 +654,14 @@ def run_qwen3_stack(args, nvq, inputs):
     (RHT on wgrad operands, SR on dy), layers 30-35 and the 151936x4096 lm_head
     in bf16 (torch.matmul).  Attention core, norms and activations are not on
     the path: the o input is the q output, the down input the up output.
-    FLOPs per step = 6 x tokens x parameters."""
+    FLOPs per step = 6 x tokens x parameters.
+
+    With the amax chain (the default; --no-amax-chain turns it off), the q and
+    up GEMMs also write their outputs' amaxes (plain and Hadamard-domain) into
+    the o and down input buffers, whose quantization then skips its amax pass."""
     import torch
     cfg = inputs.QWEN3_8B_STACK
+    chain = not args.no_amax_chain
     Tk, H = cfg["tokens"], cfg["hidden"]
     n_nv = cfg["n_layers"] - cfg["bf16_tail"]
     sign = inputs.rht_sign_vector()
@@ -700,12 +705,19 @@ def run_qwen3_stack(args, nvq, inputs):
             nvq.nvfp4_quantize(h, 3, rht_sign=sign, out_row=e["a"]["h"][0], out_col=e["a"]["h"][1])
             for n in ("q", "k", "v", "gate", "up", "o", "down"):
                 if n == "o":
-                    nvq.nvfp4_quantize(e["y"]["q"], 3, rht_sign=sign, out_row=e["a"]["attn"][0], out_col=e["a"]["attn"][1])
+                    nvq.nvfp4_quantize(e["y"]["q"], 3, rht_sign=sign, out_row=e["a"]["attn"][0], out_col=e["a"]["attn"][1],
+                                       amax_given=chain)
                 if n == "down":
-                    nvq.nvfp4_quantize(e["y"]["up"], 3, rht_sign=sign, out_row=e["a"]["mlp"][0], out_col=e["a"]["mlp"][1])
+                    nvq.nvfp4_quantize(e["y"]["up"], 3, rht_sign=sign, out_row=e["a"]["mlp"][0], out_col=e["a"]["mlp"][1],
+                                       amax_given=chain)
                 wr, wc = e["w"][n]
                 nvq.nvfp4_quantize(ws[n], 3, out_row=wr, out_col=wc)
-                nvq.gemm_tn(e["a"][src[n]][0], wr, out=e["y"][n])
+                nxt = {"q": "attn", "up": "mlp"}.get(n) if chain else None
+                if nxt:  # the output's amaxes go straight into its consumer's quantized buffers
+                    nvq.gemm_tn(e["a"][src[n]][0], wr, out=e["y"][n], rht_sign=sign, amax_out=e["a"][nxt][0].amax,
+                                amax_rht_out=e["a"][nxt][1].amax)
+                else:
+                    nvq.gemm_tn(e["a"][src[n]][0], wr, out=e["y"][n])
         tail = [torch.matmul(h if W.shape[1] == H else dys[cfg["mlp"]], W.t())
                 for l in range(n_nv, cfg["n_layers"]) for W in layers[l].values()]
         logits = torch.matmul(h, lm_head.t())
@@ -735,7 +747,9 @@ def run_qwen3_stack(args, nvq, inputs):
             "value": flop / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms,
             "dtype": "nvfp4 (layers 0-29) / bf16 (tail, lm_head)",
             "config": {"workload": "qwen3_8b_linear_stack", "tokens": Tk, "layers": cfg["n_layers"],
-                       "nvfp4_layers": n_nv, "params": params}, "tokens_per_s": Tk / (ms * 1e-3)}
+                       "nvfp4_layers": n_nv, "params": params,
+                       "amax_chain": "q -> o and up -> down: GEMM epilogue amaxes, no amax pass" if chain else "off"},
+            "tokens_per_s": Tk / (ms * 1e-3)}
 
 
 def run_single_linear(args, nvq, inputs):
@@ -796,6 +810,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip timing the CPU oracle")
     ap.add_argument("--eager", action="store_true", help="launch the step eagerly instead of replaying a CUDA graph")
     ap.add_argument("--oracle-child", type=float, default=None, help=argparse.SUPPRESS)
+    ap.add_argument("--no-amax-chain", action="store_true",
+                    help="qwen3_stack: measure every amax with its own pass instead of taking it from the producing GEMM")
     ap.add_argument("--workload", default="llama_up",
                     choices=["llama_up", "quant_sweep", "moe_grouped", "qwen3_stack", "single_linear"],
                     help="llama_up (default: the headline line) or one of the other configurations")

@@ -83,6 +83,10 @@ def _load():
                 "orc_gemm_tn_f64": (None, [P, P, i64, i64, i64, f64, P, P]),
                 "orc_gemm_tn_sampled": (None, [i32, P, P, f32, P, P, f32, i64, P, i64, P, P, P]),
                 "orc_f64_to_bf16_rne": (None, [P, i64, P]),
+                "orc_nvfp4_dequant_bf16": (None, [P, P, i64, i64, f32, P]),
+                "orc_mxfp8_dequant_bf16": (None, [P, P, i64, i64, P]),
+                "orc_identity_rows": (None, [P, i64, i64, i64, P]),
+                "orc_identity_cols": (None, [P, i64, i64, i64, P]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(lib, name)
@@ -360,3 +364,54 @@ def to_bf16_rne(v) -> np.ndarray:
     out = np.zeros(a.shape, np.uint16)
     _load().orc_f64_to_bf16_rne(_p(a), a.size, _p(out))
     return out
+
+
+# ---------------------------------------------------------------- rowwise-dequantized source / identity
+def nvfp4_dequant_bf16(codes, scales, A: float) -> np.ndarray:
+    """bf16 bit patterns of the dequantized NVFP4 operand (fp32 (E2M1*E4M3)*g, one RNE to bf16)."""
+    c = np.ascontiguousarray(codes, dtype=np.uint8)
+    s = np.ascontiguousarray(scales, dtype=np.uint8)
+    R, C = c.shape[0], c.shape[1] * 2
+    out = np.zeros((R, C), np.uint16)
+    _load().orc_nvfp4_dequant_bf16(_p(c), _p(s), R, C, A, _p(out))
+    return out
+
+
+def mxfp8_dequant_bf16(codes, scales) -> np.ndarray:
+    """bf16 bit patterns of the dequantized MXFP8 operand (E4M3*2^e exact, one RNE to bf16)."""
+    c = np.ascontiguousarray(codes, dtype=np.uint8)
+    s = np.ascontiguousarray(scales, dtype=np.uint8)
+    R, C = c.shape
+    out = np.zeros((R, C), np.uint16)
+    _load().orc_mxfp8_dequant_bf16(_p(c), _p(s), R, C, _p(out))
+    return out
+
+
+def identity_rows(x) -> np.ndarray:
+    xb = _bf16_bits(x)
+    M, K = xb.shape
+    out = np.zeros((M, K), np.uint16)
+    _load().orc_identity_rows(_p(xb), M, K, K, _p(out))
+    return out
+
+
+def identity_cols(x) -> np.ndarray:
+    """x[M,K] -> out[K, Mp] (Mp = M rounded up to 16, pad columns zero)."""
+    xb = _bf16_bits(x)
+    M, K = xb.shape
+    out = np.zeros((K, (M + 15) // 16 * 16), np.uint16)
+    _load().orc_identity_cols(_p(xb), M, K, K, _p(out))
+    return out
+
+
+def rowwise_dequantized(x, row_fmt: int, sr=None):
+    """The columnwise source of columnwise_source = "rowwise_dequantized": the
+    rowwise quantization of x (NVFP4 = 1 with its tensor amax, MXFP8 = 2)
+    dequantized to bf16.  Returns (bf16 bits [M,K], rowwise operand)."""
+    if row_fmt == 1:
+        c, s, A = nvfp4_quantize_rows(x, sr=sr)
+        return nvfp4_dequant_bf16(c, s, A), (c, s, A)
+    if row_fmt == 2:
+        c, s = mxfp8_quantize_rows(x)
+        return mxfp8_dequant_bf16(c, s), (c, s)
+    raise ValueError("the rowwise direction must be NVFP4 (1) or MXFP8 (2)")

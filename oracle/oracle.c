@@ -488,6 +488,72 @@ ORC_API void orc_mxfp8_dequant(const uint8_t* codes, const uint8_t* scales, int6
 }
 
 /* ------------------------------------------------------------------ */
+/* Rowwise-dequantized source and the identity direction ([TE]          */
+/* "Hybrid quantization", "Enable columnwise_source and hybrid recipes": */
+/* with columnwise_source = "rowwise_dequantized" the columnwise operand  */
+/* is built from dequantize(rowwise-quantized x) -- double quantization  */
+/* when the columnwise quantizer is not the identity; IdentityQuantizer  */
+/* passes the high-precision value through).                            */
+/* READING: the dequantized value is formed in fp32 -- NVFP4: the exact  */
+/* product E2M1(q) * E4M3(S), times g = A / 2688 with one rounding;      */
+/* MXFP8: E4M3(q) * 2^e, exact -- and stored in the training dtype,      */
+/* bf16, with one round to nearest even.                                 */
+/* ------------------------------------------------------------------ */
+
+ORC_API void orc_f64_to_bf16_rne(const double* v, int64_t n, uint16_t* out);
+
+/* fp32 -> bf16 bits, round to nearest even (finite inputs). */
+static uint16_t f32_to_bf16_rne(float f)
+{
+    uint16_t out;
+    double d = (double)f;
+    orc_f64_to_bf16_rne(&d, 1, &out);
+    return out;
+}
+
+/* bf16 bits of the dequantized NVFP4 operand codes[R][C/2] with compact
+ * scales[R][C/16] and tensor amax A. */
+ORC_API void orc_nvfp4_dequant_bf16(const uint8_t* codes, const uint8_t* scales, int64_t R, int64_t C, float A,
+                                    uint16_t* out)
+{
+    float g = orc_nvfp4_g(A);
+    for (int64_t r = 0; r < R; ++r)
+        for (int64_t c = 0; c < C; ++c) {
+            uint8_t byte = codes[r * (C / 2) + c / 2];
+            uint8_t q = (c & 1) ? (byte >> 4) : (byte & 15);
+            float cs = (float)(orc_e2m1_decode(q) * orc_e4m3_decode(scales[r * (C / 16) + c / 16]));  /* exact */
+            float v = cs * g;
+            out[r * C + c] = f32_to_bf16_rne(v);
+        }
+}
+
+/* bf16 bits of the dequantized MXFP8 operand codes[R][C], scales[R][C/32]. */
+ORC_API void orc_mxfp8_dequant_bf16(const uint8_t* codes, const uint8_t* scales, int64_t R, int64_t C, uint16_t* out)
+{
+    for (int64_t r = 0; r < R; ++r)
+        for (int64_t c = 0; c < C; ++c) {
+            float v = (float)(orc_e4m3_decode(codes[r * C + c]) * orc_e8m0_decode(scales[r * (C / 32) + c / 32]));
+            out[r * C + c] = f32_to_bf16_rne(v);
+        }
+}
+
+/* Identity direction: the bf16 values themselves.  Rowwise: a copy of
+ * x[M][K]; columnwise: the transpose, out[K][Mp] with Mp = M rounded up to
+ * 16 and the columns past M zero. */
+ORC_API void orc_identity_rows(const uint16_t* x, int64_t M, int64_t K, int64_t ld, uint16_t* out)
+{
+    for (int64_t i = 0; i < M; ++i)
+        for (int64_t k = 0; k < K; ++k) out[i * K + k] = x[i * ld + k];
+}
+
+ORC_API void orc_identity_cols(const uint16_t* x, int64_t M, int64_t K, int64_t ld, uint16_t* out)
+{
+    int64_t Mp = (M + 15) / 16 * 16;
+    for (int64_t k = 0; k < K; ++k)
+        for (int64_t i = 0; i < Mp; ++i) out[k * Mp + i] = (i < M) ? x[i * ld + k] : 0;
+}
+
+/* ------------------------------------------------------------------ */
 /* GEMM in TN form: out[r][c] = alpha * sum_k A[r][k] * B[c][k] + bias[c] */
 /* (fp64 accumulation of the dequantized operands).                      */
 /* ------------------------------------------------------------------ */
