@@ -69,7 +69,14 @@ typedef enum {
     NVQ_ERR_BOUNDS = 8       /* device: a checked-build index check failed */
 } nvq_status;
 
-typedef enum { NVQ_FMT_NONE = 0, NVQ_FMT_NVFP4 = 1, NVQ_FMT_MXFP8 = 2 } nvq_format;
+/* NVQ_FMT_IDENTITY: the high-precision value passed through ([TE]
+ * IdentityQuantizer): bf16 data, no scales, no amax; a quantize direction
+ * only (no GEMM takes it). */
+typedef enum { NVQ_FMT_NONE = 0, NVQ_FMT_NVFP4 = 1, NVQ_FMT_MXFP8 = 2, NVQ_FMT_IDENTITY = 3 } nvq_format;
+
+/* Source of the columnwise direction of nvq_hybrid_quantize ([TE]
+ * columnwise_source): the original tensor, or the dequantized rowwise value. */
+enum { NVQ_COL_SOURCE_ORIGINAL = 0, NVQ_COL_SOURCE_ROWWISE_DEQUANTIZED = 1 };
 
 enum { NVQ_DIR_ROW = 1, NVQ_DIR_COL = 2 };
 
@@ -100,6 +107,8 @@ typedef struct {
  *          group for grouped calls); decoded value E2M1 * E4M3 * A / 2688.
  *   MXFP8: data = E4M3 codes, rows x cols bytes; scale = E8M0 per 1x32
  *          block; amax unused (may be NULL).
+ *   IDENTITY: data = bf16 values, rows x cols x 2 bytes; scale and amax
+ *          unused (may be NULL).
  * Scales are stored in the block-scaled GEMM layout: the scale matrix
  * [rows][nb] (nb = cols / block) is padded to [ceil(rows/128)*128]
  * [ceil(nb/4)*4] and cut into 128x4 tiles of 512 bytes; tile
@@ -116,12 +125,14 @@ typedef struct {
 } nvq_qtensor;
 
 /* Bytes of data and scale storage for a [rows][cols] operand of `fmt`
- * (cols a multiple of the block: 16 for NVFP4, 32 for MXFP8). */
+ * (cols a multiple of the block: 16 for NVFP4 and IDENTITY, 32 for MXFP8;
+ * IDENTITY has no scale storage). */
 NVQ_API nvq_status nvq_query_sizes(nvq_format fmt, int64_t rows, int64_t cols, size_t* data_bytes,
                            size_t* scale_bytes);
 
 /* Columns of the columnwise (transposed) operand made from M rows: M rounded
- * up to the block (ceil, [TE] mxfp8 storage review: ceil(M/32) scales). */
+ * up to the block (ceil, [TE] mxfp8 storage review: ceil(M/32) scales; 16
+ * for NVFP4 and IDENTITY). */
 NVQ_API int64_t nvq_colwise_cols(nvq_format fmt, int64_t M);
 
 /* Amax pass ([TT] FP32 per-tensor scale).  amax_out[0] = max |x| over
@@ -171,10 +182,22 @@ NVQ_API nvq_status nvq_mxfp8_quantize(const void* x, int64_t M, int64_t K, int64
                               nvq_qtensor* row, nvq_qtensor* col, nvq_stream stream);
 
 /* Hybrid quantization ([TE] HybridQuantizer): rowwise in row_fmt and
- * columnwise in col_fmt, both from the original bf16 (col_source must be 0,
- * "original"), from one read of x.  A direction whose format is
- * NVQ_FMT_NONE is skipped (usage flag).  rht_col / sr apply to NVFP4
- * directions only.  hybrid(F, F) is bitwise equal to the single-format call. */
+ * columnwise in col_fmt, each NVFP4, MXFP8 or IDENTITY.  A direction whose
+ * format is NVQ_FMT_NONE is skipped (usage flag).  rht_col / sr apply to
+ * NVFP4 directions only.  hybrid(F, F) is bitwise equal to the single-format
+ * call.  An IDENTITY direction stores the bf16 values: rowwise a copy
+ * [M][K], columnwise the transpose [K][nvq_colwise_cols(IDENTITY, M)].
+ *   col_source = NVQ_COL_SOURCE_ORIGINAL: both directions from the original
+ *     x, from one read of it.
+ *   col_source = NVQ_COL_SOURCE_ROWWISE_DEQUANTIZED ([TE] "Enable
+ *     columnwise_source and hybrid recipes": the backward operand is built
+ *     from dequantize(rowwise-quantized x), double quantization unless the
+ *     columnwise quantizer is the identity): row_fmt must be NVFP4 or MXFP8;
+ *     the columnwise direction quantizes (or, IDENTITY, stores) the
+ *     dequantized rowwise value x^ = bf16_rn(fp32 (E2M1 * E4M3) * (A / 2688))
+ *     (NVFP4, A the rowwise amax) or bf16_rn(E4M3 * 2^e) (MXFP8, exact).  An
+ *     NVFP4 columnwise direction then takes its amax over x^ (or T(x^)), which
+ *     costs a second pass over x.  Not available for grouped tensors. */
 NVQ_API nvq_status nvq_hybrid_quantize(const void* x, int64_t M, int64_t K, int64_t ld,
                                nvq_format row_fmt, nvq_format col_fmt, int col_source,
                                const nvq_rht* rht_col, const nvq_sr* sr, nvq_qtensor* row,

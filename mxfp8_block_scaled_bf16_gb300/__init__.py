@@ -22,7 +22,8 @@ import torch
 from . import build as _build
 
 __all__ = [
-    "NVFP4", "MXFP8", "NONE", "DIR_ROW", "DIR_COL", "AMAX_GIVEN", "NvqError", "QTensor", "lib", "load",
+    "NVFP4", "MXFP8", "IDENTITY", "NONE", "DIR_ROW", "DIR_COL", "AMAX_GIVEN", "COL_SOURCE_ORIGINAL",
+    "COL_SOURCE_ROWWISE_DEQUANTIZED", "NvqError", "QTensor", "lib", "load",
     "alloc_qtensor", "query_sizes", "colwise_cols", "amax", "nvfp4_quantize", "mxfp8_quantize",
     "hybrid_quantize", "gemm_tn", "nvfp4_linear_fwd", "nvfp4_linear_bwd_quantize",
     "nvfp4_linear_dgrad", "nvfp4_linear_wgrad", "grouped_padded_rows", "grouped_hybrid_quantize",
@@ -31,7 +32,8 @@ __all__ = [
     "EXPORTED_SYMBOLS",
 ]
 
-NONE, NVFP4, MXFP8 = 0, 1, 2
+NONE, NVFP4, MXFP8, IDENTITY = 0, 1, 2, 3
+COL_SOURCE_ORIGINAL, COL_SOURCE_ROWWISE_DEQUANTIZED = 0, 1
 DIR_ROW, DIR_COL = 1, 2
 AMAX_GIVEN = 1
 MAX_GROUPS = 256
@@ -150,8 +152,14 @@ class QTensor:
     amax: Optional[torch.Tensor]
 
     def c(self) -> _QT:
-        return _QT(self.fmt, self.data.data_ptr(), self.scale.data_ptr(),
+        return _QT(self.fmt, self.data.data_ptr(), self.scale.data_ptr() if self.scale is not None else None,
                    self.amax.data_ptr() if self.amax is not None else None, self.rows, self.cols)
+
+    def bf16(self) -> torch.Tensor:
+        """The values of an IDENTITY operand as a bf16 [rows, cols] view."""
+        if self.fmt != IDENTITY:
+            raise ValueError("only an IDENTITY operand holds bf16 values")
+        return self.data[: self.rows * self.cols * 2].view(torch.bfloat16).view(self.rows, self.cols)
 
 
 def query_sizes(fmt: int, rows: int, cols: int):
@@ -167,7 +175,7 @@ def colwise_cols(fmt: int, M: int) -> int:
 def alloc_qtensor(fmt: int, rows: int, cols: int, n_amax: int = 1, device="cuda") -> QTensor:
     db, sb = query_sizes(fmt, rows, cols)
     data = torch.empty(max(db, 16), dtype=torch.uint8, device=device)
-    scale = torch.empty(max(sb, 16), dtype=torch.uint8, device=device)
+    scale = torch.empty(max(sb, 16), dtype=torch.uint8, device=device) if fmt != IDENTITY else None
     amax = torch.empty(max(n_amax, 1), dtype=torch.float32, device=device) if fmt == NVFP4 else None
     return QTensor(fmt, rows, cols, data, scale, amax)
 
@@ -205,13 +213,16 @@ def amax(x: torch.Tensor, rht_sign=None, stream=None):
 
 
 def hybrid_quantize(x: torch.Tensor, row_fmt: int, col_fmt: int, rht_sign=None, sr=None, stream=None,
-                    out_row: Optional[QTensor] = None, out_col: Optional[QTensor] = None):
-    """Rowwise in ``row_fmt`` and columnwise in ``col_fmt`` from one read of x."""
+                    out_row: Optional[QTensor] = None, out_col: Optional[QTensor] = None,
+                    col_source: int = COL_SOURCE_ORIGINAL):
+    """Rowwise in ``row_fmt`` and columnwise in ``col_fmt`` (NVFP4, MXFP8 or
+    IDENTITY); the columnwise source is the original x or, with
+    COL_SOURCE_ROWWISE_DEQUANTIZED, the dequantized rowwise value."""
     M, K, ld = _bf16_2d(x)
     row = out_row or (alloc_qtensor(row_fmt, M, K, device=x.device) if row_fmt else None)
     col = out_col or (alloc_qtensor(col_fmt, K, colwise_cols(col_fmt, M), device=x.device) if col_fmt else None)
     rc, cc = (row.c() if row else None), (col.c() if col else None)
-    _check(load().nvq_hybrid_quantize(_ptr(x), M, K, ld, row_fmt, col_fmt, 0, _rht(rht_sign), _sr(sr),
+    _check(load().nvq_hybrid_quantize(_ptr(x), M, K, ld, row_fmt, col_fmt, col_source, _rht(rht_sign), _sr(sr),
                                       ctypes.byref(rc) if rc else None, ctypes.byref(cc) if cc else None,
                                       _stream(stream)), "nvq_hybrid_quantize")
     return row, col

@@ -25,8 +25,8 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 # must round exactly as written (no multiply-add contraction).
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "--fmad=false", "-Xcompiler", "-fPIC",
               "-Xcompiler", "-fvisibility=hidden", "-I", INCLUDE]
-SOURCES = ["api.cu", "quantize.cu", "gemm.cu", "gemm2.cu"]
-HEADERS = ["nvq_device.cuh", "nvq_kernels.h", "gemm_epilogue.cuh"]
+SOURCES = ["api.cu", "quantize.cu", "quantize_hybrid.cu", "gemm.cu", "gemm2.cu"]
+HEADERS = ["nvq_device.cuh", "nvq_kernels.h", "gemm_epilogue.cuh", "quantize_kernel.cuh"]
 
 
 def _nvcc() -> str:

@@ -108,23 +108,27 @@ nvq_status make_operand_map(CUtensorMap* map, const void* data, int64_t rows, in
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 inline int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
-inline int block_of(nvq_format f) { return f == NVQ_FMT_NVFP4 ? 16 : 32; }
+// block of the format's scales; the identity (bf16) direction pads its
+// columnwise storage to 16 like NVFP4 and has no scales
+inline int block_of(nvq_format f) { return f == NVQ_FMT_MXFP8 ? 32 : 16; }
 inline bool valid_fmt(nvq_format f) { return f == NVQ_FMT_NVFP4 || f == NVQ_FMT_MXFP8; }
+inline bool valid_qfmt(nvq_format f) { return valid_fmt(f) || f == NVQ_FMT_IDENTITY; }
 
 int64_t data_bytes(nvq_format f, int64_t rows, int64_t cols)
 {
-    return f == NVQ_FMT_NVFP4 ? rows * (cols / 2) : rows * cols;
+    return f == NVQ_FMT_NVFP4 ? rows * (cols / 2) : f == NVQ_FMT_IDENTITY ? rows * cols * 2 : rows * cols;
 }
 
 int64_t scale_ctiles(nvq_format f, int64_t cols) { return ceil_div(cols / block_of(f), 4); }
 
 nvq_status check_qtensor(const nvq_qtensor* t, nvq_format fmt, int64_t rows, int64_t cols)
 {
-    if (!t || !t->data || !t->scale) return NVQ_ERR_NULL;
+    if (!t || !t->data || (!t->scale && fmt != NVQ_FMT_IDENTITY)) return NVQ_ERR_NULL;
     if (t->fmt != fmt) return NVQ_ERR_UNSUPPORTED;
     if (fmt == NVQ_FMT_NVFP4 && !t->amax) return NVQ_ERR_NULL;
     if (t->rows != rows || t->cols != cols) return NVQ_ERR_SHAPE;
-    if (!aligned16(t->data) || !aligned16(t->scale) || (fmt == NVQ_FMT_NVFP4 && (reinterpret_cast<uintptr_t>(t->amax) & 3)))
+    if (!aligned16(t->data) || (fmt != NVQ_FMT_IDENTITY && !aligned16(t->scale)) ||
+        (fmt == NVQ_FMT_NVFP4 && (reinterpret_cast<uintptr_t>(t->amax) & 3)))
         return NVQ_ERR_ALIGN;
     return NVQ_OK;
 }
@@ -146,10 +150,17 @@ uint32_t sign_mask(const nvq_rht* rht, bool* ok)
 // of M rows (outputs unpadded: row rows = M, col cols = colwise_cols(M)).
 nvq_status quantize_impl(const void* x, int64_t M, int64_t K, int64_t ld, const int64_t* group_rows, int G,
                          nvq_format row_fmt, nvq_format col_fmt, const nvq_rht* rht_col, const nvq_sr* sr,
-                         nvq_qtensor* row, nvq_qtensor* col, cudaStream_t stream, bool amax_given = false)
+                         nvq_qtensor* row, nvq_qtensor* col, cudaStream_t stream, bool amax_given = false,
+                         int col_source = NVQ_COL_SOURCE_ORIGINAL)
 {
-    if (row_fmt != NVQ_FMT_NONE && !valid_fmt(row_fmt)) return NVQ_ERR_UNSUPPORTED;
-    if (col_fmt != NVQ_FMT_NONE && !valid_fmt(col_fmt)) return NVQ_ERR_UNSUPPORTED;
+    if (row_fmt != NVQ_FMT_NONE && !valid_qfmt(row_fmt)) return NVQ_ERR_UNSUPPORTED;
+    if (col_fmt != NVQ_FMT_NONE && !valid_qfmt(col_fmt)) return NVQ_ERR_UNSUPPORTED;
+    const bool dq = col_source == NVQ_COL_SOURCE_ROWWISE_DEQUANTIZED;
+    if (col_source != NVQ_COL_SOURCE_ORIGINAL && !dq) return NVQ_ERR_UNSUPPORTED;
+    // the rowwise-dequantized source needs a quantized rowwise direction
+    if (dq && (!valid_fmt(row_fmt) || col_fmt == NVQ_FMT_NONE)) return NVQ_ERR_UNSUPPORTED;
+    const bool hybrid_kernel = dq || row_fmt == NVQ_FMT_IDENTITY || col_fmt == NVQ_FMT_IDENTITY;
+    if (hybrid_kernel && group_rows) return NVQ_ERR_UNSUPPORTED;
     if (K < 0 || ld < K || (ld % 8) != 0) return NVQ_ERR_SHAPE;
     if (!aligned16(x)) return NVQ_ERR_ALIGN;
     if ((row_fmt != NVQ_FMT_NONE && K % block_of(row_fmt)) || K % 16) return NVQ_ERR_SHAPE;
@@ -245,17 +256,18 @@ nvq_status quantize_impl(const void* x, int64_t M, int64_t K, int64_t ld, const 
         if (e == cudaSuccess && do_col && K > 0) {
             size_t db = (size_t)data_bytes(col_fmt, K, col_cols);
             if (db) e = cudaMemsetAsync(col->data, 0, db, stream);
-            size_t sb = (size_t)(round_up(K, 128) * round_up(col_cols / block_of(col_fmt), 4));
+            size_t sb = col_fmt == NVQ_FMT_IDENTITY ? 0 : (size_t)(round_up(K, 128) * round_up(col_cols / block_of(col_fmt), 4));
             if (e == cudaSuccess && sb) e = cudaMemsetAsync(col->scale, 0, sb, stream);
         }
         return cuda_status(e);
     }
     if (any_nv && !amax_given) {
         // amax pass: plain amax for NVFP4 rowwise (and NVFP4 columnwise without
-        // RHT), Hadamard-domain amax for NVFP4 columnwise with RHT
+        // RHT), Hadamard-domain amax for NVFP4 columnwise with RHT; a
+        // rowwise-dequantized columnwise direction measures its own below
         float* plain_row = row_fmt == NVQ_FMT_NVFP4 ? row->amax : nullptr;
-        float* plain_col = (col_fmt == NVQ_FMT_NVFP4 && !rht) ? col->amax : nullptr;
-        float* rht_out = (col_fmt == NVQ_FMT_NVFP4 && rht) ? col->amax : nullptr;
+        float* plain_col = (col_fmt == NVQ_FMT_NVFP4 && !rht && !dq) ? col->amax : nullptr;
+        float* rht_out = (col_fmt == NVQ_FMT_NVFP4 && rht && !dq) ? col->amax : nullptr;
         cudaError_t e = cudaSuccess;
         if (plain_row) e = cudaMemsetAsync(plain_row, 0, sizeof(float) * nG, stream);
         if (e == cudaSuccess && plain_col) e = cudaMemsetAsync(plain_col, 0, sizeof(float) * nG, stream);
@@ -264,9 +276,27 @@ nvq_status quantize_impl(const void* x, int64_t M, int64_t K, int64_t ld, const 
         a.amax_out[0] = plain_row ? plain_row : plain_col;
         a.amax_out[1] = plain_row ? plain_col : nullptr;
         a.amax_rht_out = rht_out;
-        if (launch_amax(a, row_tiles, stream) != cudaSuccess) return NVQ_ERR_CUDA;
+        if ((plain_row || plain_col || rht_out) && launch_amax(a, row_tiles, stream) != cudaSuccess)
+            return NVQ_ERR_CUDA;
+        a.amax_out[0] = a.amax_out[1] = a.amax_rht_out = nullptr;
     }
-    return cuda_status(launch_quantize(a, (int)row_fmt, (int)col_fmt, rht, sr != nullptr, row_tiles, stream));
+    if (!hybrid_kernel)
+        return cuda_status(launch_quantize(a, (int)row_fmt, (int)col_fmt, rht, sr != nullptr, row_tiles, stream));
+    if (dq && col_fmt == NVQ_FMT_NVFP4) {
+        // The columnwise scale needs the amax of the dequantized values before
+        // any block is quantized: a first pass writes the rowwise operand and
+        // that amax, a second recomputes the dequantized values (the same
+        // rowwise arithmetic) and quantizes them columnwise.
+        if (cudaMemsetAsync(col->amax, 0, sizeof(float), stream) != cudaSuccess) return NVQ_ERR_CUDA;
+        QuantArgs a1 = a;
+        a1.col_data = nullptr;
+        a1.dq_amax = col->amax;
+        if (launch_quantize_hybrid(a1, (int)row_fmt, (int)col_fmt, rht, sr != nullptr, true, row_tiles, stream) !=
+            cudaSuccess)
+            return NVQ_ERR_CUDA;
+        a.row_data = nullptr;
+    }
+    return cuda_status(launch_quantize_hybrid(a, (int)row_fmt, (int)col_fmt, rht, sr != nullptr, dq, row_tiles, stream));
 }
 
 // Test hook for the bounded waits: with NVQ_DEBUG_DROP_TMA=1 in the
@@ -437,16 +467,16 @@ extern "C" {
 nvq_status nvq_query_sizes(nvq_format fmt, int64_t rows, int64_t cols, size_t* db, size_t* sb)
 {
     if (!db || !sb) return NVQ_ERR_NULL;
-    if (!valid_fmt(fmt)) return NVQ_ERR_UNSUPPORTED;
+    if (!valid_qfmt(fmt)) return NVQ_ERR_UNSUPPORTED;
     if (rows < 0 || cols < 0 || cols % block_of(fmt)) return NVQ_ERR_SHAPE;
     *db = (size_t)data_bytes(fmt, rows, cols);
-    *sb = (size_t)(round_up(rows, 128) * round_up(cols / block_of(fmt), 4));
+    *sb = fmt == NVQ_FMT_IDENTITY ? 0 : (size_t)(round_up(rows, 128) * round_up(cols / block_of(fmt), 4));
     return NVQ_OK;
 }
 
 int64_t nvq_colwise_cols(nvq_format fmt, int64_t M)
 {
-    if (!valid_fmt(fmt) || M < 0) return -1;
+    if (!valid_qfmt(fmt) || M < 0) return -1;
     return round_up(M, block_of(fmt));
 }
 
@@ -505,9 +535,8 @@ nvq_status nvq_hybrid_quantize(const void* x, int64_t M, int64_t K, int64_t ld, 
                                nvq_format col_fmt, int col_source, const nvq_rht* rht_col, const nvq_sr* sr,
                                nvq_qtensor* row, nvq_qtensor* col, nvq_stream stream)
 {
-    if (col_source != 0) return NVQ_ERR_UNSUPPORTED;
     return quantize_impl(x, M, K, ld, nullptr, 1, row_fmt, col_fmt, rht_col, sr, row, col,
-                         reinterpret_cast<cudaStream_t>(stream));
+                         reinterpret_cast<cudaStream_t>(stream), false, col_source);
 }
 
 nvq_status nvq_gemm_tn(const nvq_qtensor* A, const nvq_qtensor* B, const void* bias, void* C, int64_t ldc,

@@ -41,6 +41,9 @@ struct QuantArgs {
     // amax pass outputs (per group), any may be NULL
     float* amax_out[2];
     float* amax_rht_out;
+    // rowwise-dequantized source: the pass that measures the columnwise
+    // source's amax (plain, or Hadamard-domain with RHT) writes it here
+    float* dq_amax;
     // RHT and SR
     uint32_t rht_sign_mask;  // bit i set: sign[i] == -1
     uint32_t sr_offset;
@@ -51,6 +54,10 @@ struct QuantArgs {
 cudaError_t launch_amax(const QuantArgs& a, int64_t row_tiles, cudaStream_t s);
 cudaError_t launch_quantize(const QuantArgs& a, int row_fmt, int col_fmt, bool rht, bool sr,
                             int64_t row_tiles, cudaStream_t s);
+// Variants with an identity direction (format 3) or the rowwise-dequantized
+// columnwise source (dq): quantize_hybrid.cu.
+cudaError_t launch_quantize_hybrid(const QuantArgs& a, int row_fmt, int col_fmt, bool rht, bool sr, bool dq,
+                                   int64_t row_tiles, cudaStream_t s);
 
 // ------------------------------------------------------------------ GEMM
 // One GEMM problem (or one group of a grouped GEMM) in TN form.

@@ -47,6 +47,8 @@ def test_status_strings(lib):
 
 def test_query_sizes():
     assert nvq.query_sizes(nvq.NVFP4, 256, 512) == (256 * 256, 256 * 32)
+    assert nvq.query_sizes(nvq.IDENTITY, 40, 48) == (40 * 48 * 2, 0)
+    assert nvq.colwise_cols(nvq.IDENTITY, 40) == 48
     assert nvq.query_sizes(nvq.MXFP8, 200, 96) == (200 * 96, 256 * 4)
     assert nvq.colwise_cols(nvq.NVFP4, 40) == 48
     assert nvq.colwise_cols(nvq.MXFP8, 48) == 64
@@ -84,8 +86,16 @@ def test_host_validation_before_any_launch(lib):
     assert lib.nvq_nvfp4_quantize(16, 128, 256, 256, 1, None, None, QTP(_qt(1, 128, 256, amax=None)), None, None) == 1
     # MXFP8 rowwise needs K % 32
     assert lib.nvq_mxfp8_quantize(16, 128, 48, 48, 1, QTP(_qt(2, 128, 48)), None, None) == 2
-    # hybrid: only columnwise_source = original
-    assert lib.nvq_hybrid_quantize(16, 128, 256, 256, 1, 2, 1, None, None, QTP(r), QTP(c), None) == 5
+    # hybrid: columnwise_source must be original (0) or rowwise_dequantized (1), and the
+    # rowwise-dequantized source needs a quantized rowwise direction
+    assert lib.nvq_hybrid_quantize(16, 128, 256, 256, 1, 2, 2, None, None, QTP(r), QTP(c), None) == 5
+    assert lib.nvq_hybrid_quantize(16, 128, 256, 256, 0, 2, 1, None, None, None, QTP(c), None) == 5
+    assert lib.nvq_hybrid_quantize(16, 128, 256, 256, 3, 2, 1, None, None, QTP(_qt(3, 128, 256)), QTP(c), None) == 5
+    # identity is a quantize direction only: no grouped identity, no identity GEMM
+    rows2 = (ctypes.c_int64 * 2)(3, 5)
+    assert lib.nvq_grouped_hybrid_quantize(16, 256, 256, rows2, 2, 3, 2, QTP(_qt(3, 256, 256)), QTP(c), None, None,
+                                           None) == 5
+    assert lib.nvq_gemm_tn(QTP(_qt(3, 128, 256)), QTP(_qt(3, 128, 256)), None, 16, 128, 0, None) == 5
     # bad RHT sign vector
     bad = nvq._RHT((ctypes.c_int8 * 16)(*([1] * 15 + [0])))
     assert lib.nvq_nvfp4_quantize(16, 128, 256, 256, 3, QTP(bad), None, QTP(r), QTP(c), None) == 2
