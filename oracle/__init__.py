@@ -87,6 +87,9 @@ def _load():
                 "orc_mxfp8_dequant_bf16": (None, [P, P, i64, i64, P]),
                 "orc_identity_rows": (None, [P, i64, i64, i64, P]),
                 "orc_identity_cols": (None, [P, i64, i64, i64, P]),
+                "orc_nvfp4_quantize_rows_rowscaled": (None, [P, i64, i64, i64, P, P, P]),
+                "orc_nvfp4_dequant_rowscaled": (None, [P, P, i64, i64, P, P]),
+                "orc_gemm_tn_sampled_rowscaled": (None, [P, P, P, P, P, f32, i64, i64, P, P, P]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(lib, name)
@@ -415,3 +418,43 @@ def rowwise_dequantized(x, row_fmt: int, sr=None):
         c, s = mxfp8_quantize_rows(x)
         return mxfp8_dequant_bf16(c, s), (c, s)
     raise ValueError("the rowwise direction must be NVFP4 (1) or MXFP8 (2)")
+
+
+# ---------------------------------------------------------------- row-scaled NVFP4
+def nvfp4_quantize_rows_rowscaled(x):
+    """Row-scaled NVFP4 of bf16 x[M,K] (a per-row FP32 outer scale) ->
+    (codes u8[M,K/2], compact scales u8[M,K/16], per-row amax f32[M])."""
+    xb = _bf16_bits(x)
+    M, K = xb.shape
+    if K % 16:
+        raise ValueError("K must be a multiple of 16")
+    codes = np.zeros((M, K // 2), np.uint8)
+    scales = np.zeros((M, K // 16), np.uint8)
+    amax_rows = np.zeros(M, np.float32)
+    _load().orc_nvfp4_quantize_rows_rowscaled(_p(xb), M, K, K, _p(codes), _p(scales), _p(amax_rows))
+    return codes, scales, amax_rows
+
+
+def nvfp4_dequant_rowscaled(codes, scales, amax_rows) -> np.ndarray:
+    c = np.ascontiguousarray(codes, dtype=np.uint8)
+    s = np.ascontiguousarray(scales, dtype=np.uint8)
+    a = np.ascontiguousarray(amax_rows, dtype=np.float32)
+    R, C = c.shape[0], c.shape[1] * 2
+    out = np.zeros((R, C), np.float64)
+    _load().orc_nvfp4_dequant_rowscaled(_p(c), _p(s), R, C, _p(a), _p(out))
+    return out
+
+
+def gemm_tn_sampled_rowscaled(a_codes, a_scales, a_amax_rows, b_codes, b_scales, b_amax, K, rows, cols):
+    """Sampled fp64 outputs of A (row-scaled NVFP4) x B^T (NVFP4, tensor amax b_amax)."""
+    ga = np.array([nvfp4_g(float(v)) for v in np.asarray(a_amax_rows, np.float32)], np.float32)
+    ac = np.ascontiguousarray(a_codes, dtype=np.uint8)
+    asc = np.ascontiguousarray(a_scales, dtype=np.uint8)
+    bc = np.ascontiguousarray(b_codes, dtype=np.uint8)
+    bsc = np.ascontiguousarray(b_scales, dtype=np.uint8)
+    r = np.ascontiguousarray(rows, dtype=np.int64)
+    c = np.ascontiguousarray(cols, dtype=np.int64)
+    out = np.zeros(r.size, np.float64)
+    _load().orc_gemm_tn_sampled_rowscaled(_p(ac), _p(asc), _p(ga), _p(bc), _p(bsc), float(nvfp4_g(b_amax)), K,
+                                          r.size, _p(r), _p(c), _p(out))
+    return out

@@ -376,6 +376,45 @@ ORC_API void orc_nvfp4_quantize_cols(const uint16_t* x, int64_t M, int64_t K, in
 }
 
 /* ------------------------------------------------------------------ */
+/* Row-scaled NVFP4 ([TE] "Hybrid quantization", Description: the grouped */
+/* GEMM recipe's input quantizer NVFP4Quantizer(row_scaled_nvfp4=True)).  */
+/* READING: the FP32 outer scale is per row instead of per tensor: row r   */
+/* has its own amax A_r = max_k |x[r][k]|, which takes the place of the    */
+/* tensor amax in every step above (s_enc, the block scale, the element    */
+/* factor), and decodes with g_r = A_r / 2688.  Rowwise only.              */
+/* ------------------------------------------------------------------ */
+
+ORC_API void orc_nvfp4_dequant(const uint8_t* codes, const uint8_t* scales, int64_t R, int64_t C,
+                               float g, double* out);
+
+ORC_API void orc_nvfp4_quantize_rows_rowscaled(const uint16_t* x, int64_t M, int64_t K, int64_t ld,
+                                               uint8_t* codes, uint8_t* scales, float* amax_rows)
+{
+    orc_sr rtn = {0, 0, 0};
+    int64_t nb = K / 16;
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < M; ++i) {
+        float A = orc_amax(x + i * ld, 1, K, ld);
+        amax_rows[i] = A;
+        for (int64_t j = 0; j < nb; ++j) {
+            float u[16];
+            uint8_t q[16];
+            for (int t = 0; t < 16; ++t) u[t] = bf16_to_f32(x[i * ld + 16 * j + t]);
+            nvfp4_block(u, A, &rtn, 0, (uint64_t)(i * K + 16 * j), q, &scales[i * nb + j]);
+            for (int t = 0; t < 8; ++t)
+                codes[i * (K / 2) + 8 * j + t] = (uint8_t)(q[2 * t] | (q[2 * t + 1] << 4));
+        }
+    }
+}
+
+ORC_API void orc_nvfp4_dequant_rowscaled(const uint8_t* codes, const uint8_t* scales, int64_t R, int64_t C,
+                                         const float* amax_rows, double* out)
+{
+    for (int64_t r = 0; r < R; ++r)
+        orc_nvfp4_dequant(codes + r * (C / 2), scales + r * (C / 16), 1, C, orc_nvfp4_g(amax_rows[r]), out + r * C);
+}
+
+/* ------------------------------------------------------------------ */
 /* MXFP8 ([TE] mxfp8 storage review: 32-element blocks, E8M0 scale,     */
 /* ceil(M/32) columnwise scale rows).  READING (OCP MX): with b the     */
 /* block amax, e = clamp(floor(log2 b) - 8, -127, 127) (8 = emax of     */
@@ -597,6 +636,22 @@ ORC_API void orc_gemm_tn_sampled(int fmt, const uint8_t* a_codes, const uint8_t*
             acc += deq_elem(fmt, a_codes, a_scales, rows[s], k, K, g_a) *
                    deq_elem(fmt, b_codes, b_scales, cols[s], k, K, g_b);
         out[s] = acc + (bias ? bias[cols[s]] : 0.0);
+    }
+}
+
+/* orc_gemm_tn_sampled for a row-scaled NVFP4 A (decode factor g_a_rows[r]
+ * for row r) and an NVFP4 B with decode factor g_b. */
+ORC_API void orc_gemm_tn_sampled_rowscaled(const uint8_t* a_codes, const uint8_t* a_scales, const float* g_a_rows,
+                                           const uint8_t* b_codes, const uint8_t* b_scales, float g_b, int64_t K,
+                                           int64_t n_samples, const int64_t* rows, const int64_t* cols, double* out)
+{
+#pragma omp parallel for schedule(dynamic, 16)
+    for (int64_t s = 0; s < n_samples; ++s) {
+        double acc = 0.0;
+        for (int64_t k = 0; k < K; ++k)
+            acc += deq_elem(1, a_codes, a_scales, rows[s], k, K, g_a_rows[rows[s]]) *
+                   deq_elem(1, b_codes, b_scales, cols[s], k, K, g_b);
+        out[s] = acc;
     }
 }
 
