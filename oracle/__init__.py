@@ -88,6 +88,7 @@ def _load():
                 "orc_identity_rows": (None, [P, i64, i64, i64, P]),
                 "orc_identity_cols": (None, [P, i64, i64, i64, P]),
                 "orc_nvfp4_quantize_rows_rowscaled": (None, [P, i64, i64, i64, P, P, P]),
+                "orc_nvfp4_quantize_cols_2d": (None, [P, i64, i64, i64, f32, P, P]),
                 "orc_nvfp4_dequant_rowscaled": (None, [P, P, i64, i64, P, P]),
                 "orc_gemm_tn_sampled_rowscaled": (None, [P, P, P, P, P, f32, i64, i64, P, P, P]),
             }
@@ -458,3 +459,20 @@ def gemm_tn_sampled_rowscaled(a_codes, a_scales, a_amax_rows, b_codes, b_scales,
     _load().orc_gemm_tn_sampled_rowscaled(_p(ac), _p(asc), _p(ga), _p(bc), _p(bsc), float(nvfp4_g(b_amax)), K,
                                           r.size, _p(r), _p(c), _p(out))
     return out
+
+
+# ---------------------------------------------------------------- NVFP4 2D (16 x 16) columnwise scaling
+def nvfp4_quantize_cols_2d(x, A: float | None = None):
+    """Columnwise NVFP4 of bf16 x[M,K] with one scale per 16 x 16 tile ->
+    (codes u8[K, Mp/2], compact scales u8[K, Mp/16], A); K % 16 == 0."""
+    xb = _bf16_bits(x)
+    M, K = xb.shape
+    if K % 16:
+        raise ValueError("K must be a multiple of 16")
+    if A is None:
+        A = amax(xb)
+    nb = (M + 15) // 16
+    codes = np.zeros((K, nb * 8), np.uint8)
+    scales = np.zeros((K, nb), np.uint8)
+    _load().orc_nvfp4_quantize_cols_2d(_p(xb), M, K, K, A, _p(codes), _p(scales))
+    return codes, scales, A

@@ -376,6 +376,49 @@ ORC_API void orc_nvfp4_quantize_cols(const uint16_t* x, int64_t M, int64_t K, in
 }
 
 /* ------------------------------------------------------------------ */
+/* NVFP4 2D block scaling, columnwise ([TE] "Hybrid quantization",        */
+/* timeline: "[Common] Enable NVFP4 2D block scaling in columnwise only").  */
+/* READING: the columnwise direction of x[M][K] takes one E4M3 scale per   */
+/* 16 x 16 tile (rows 16j.., columns 16c..) from the tile's amax, with the */
+/* per-tensor recipe otherwise unchanged (s_enc, the block scale from the  */
+/* amax, the element factor, RTN); each of the tile's 16 columnwise        */
+/* 1 x 16 blocks is stored with that scale.  The rowwise direction keeps   */
+/* 1 x 16 blocks.  Rows past M read as zero; K % 16 == 0.                  */
+/* ------------------------------------------------------------------ */
+
+ORC_API void orc_nvfp4_quantize_cols_2d(const uint16_t* x, int64_t M, int64_t K, int64_t ld, float A,
+                                        uint8_t* codes, uint8_t* scales)
+{
+    int64_t nb = (M + 15) / 16, Mp = nb * 16;
+#pragma omp parallel for schedule(static)
+    for (int64_t j = 0; j < nb; ++j)
+        for (int64_t c = 0; c < K / 16; ++c) {
+            float tile[16][16];  /* [column in tile][row in block] */
+            float b = 0.0f;
+            for (int kk = 0; kk < 16; ++kk) {
+                load_col_block(x, M, ld, 16 * c + kk, j, tile[kk]);
+                for (int t = 0; t < 16; ++t)
+                    if (fabsf(tile[kk][t]) > b) b = fabsf(tile[kk][t]);
+            }
+            uint8_t S = 0;
+            if (b != 0.0f && A != 0.0f) S = orc_e4m3_encode_rn(b * (448.0f / A));
+            float e = 0.0f;
+            if (S != 0) {
+                e = orc_nvfp4_s_enc(A) / (float)orc_e4m3_decode(S);
+                if (isinf(e)) e = FLT_MAX;
+            }
+            for (int kk = 0; kk < 16; ++kk) {
+                int64_t k = 16 * c + kk;
+                uint8_t q[16];
+                for (int t = 0; t < 16; ++t) q[t] = orc_e2m1_encode_rn(tile[kk][t] * e);
+                for (int t = 0; t < 8; ++t)
+                    codes[k * (Mp / 2) + 8 * j + t] = (uint8_t)(q[2 * t] | (q[2 * t + 1] << 4));
+                scales[k * nb + j] = S;
+            }
+        }
+}
+
+/* ------------------------------------------------------------------ */
 /* Row-scaled NVFP4 ([TE] "Hybrid quantization", Description: the grouped */
 /* GEMM recipe's input quantizer NVFP4Quantizer(row_scaled_nvfp4=True)).  */
 /* READING: the FP32 outer scale is per row instead of per tensor: row r   */
