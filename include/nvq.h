@@ -71,8 +71,20 @@ typedef enum {
 
 /* NVQ_FMT_IDENTITY: the high-precision value passed through ([TE]
  * IdentityQuantizer): bf16 data, no scales, no amax; a quantize direction
- * only (no GEMM takes it). */
-typedef enum { NVQ_FMT_NONE = 0, NVQ_FMT_NVFP4 = 1, NVQ_FMT_MXFP8 = 2, NVQ_FMT_IDENTITY = 3 } nvq_format;
+ * only (no GEMM takes it).
+ * NVQ_FMT_NVFP4_ROWSCALED: NVFP4 with an FP32 outer scale per row instead of
+ * per tensor ([TE] Description, the grouped GEMM recipe's input quantizer
+ * NVFP4Quantizer(row_scaled_nvfp4=True)): row r's amax A_r takes the tensor
+ * amax's place in every step of the NVFP4 recipe and it decodes as
+ * E2M1 * E4M3 * (A_r / 2688).  A rowwise direction only; a GEMM takes it as A
+ * with an NVFP4 B (alpha per output row). */
+typedef enum {
+    NVQ_FMT_NONE = 0,
+    NVQ_FMT_NVFP4 = 1,
+    NVQ_FMT_MXFP8 = 2,
+    NVQ_FMT_IDENTITY = 3,
+    NVQ_FMT_NVFP4_ROWSCALED = 4
+} nvq_format;
 
 /* Source of the columnwise direction of nvq_hybrid_quantize ([TE]
  * columnwise_source): the original tensor, or the dequantized rowwise value. */
@@ -109,6 +121,8 @@ typedef struct {
  *          block; amax unused (may be NULL).
  *   IDENTITY: data = bf16 values, rows x cols x 2 bytes; scale and amax
  *          unused (may be NULL).
+ *   NVFP4_ROWSCALED: as NVFP4, with amax = device float[rows], row r's amax
+ *          (grouped storage: one per padded row, 0 for pad rows).
  * Scales are stored in the block-scaled GEMM layout: the scale matrix
  * [rows][nb] (nb = cols / block) is padded to [ceil(rows/128)*128]
  * [ceil(nb/4)*4] and cut into 128x4 tiles of 512 bytes; tile
@@ -167,7 +181,15 @@ enum {
      * call, as the producer of x wrote them (nvq_gemm_tn_amax); the amax pass
      * is skipped and x is read once.  The codes equal those of the measured
      * call when the given amaxes equal the measured ones. */
-    NVQ_AMAX_GIVEN = 1
+    NVQ_AMAX_GIVEN = 1,
+    /* The NVFP4 columnwise direction takes one E4M3 scale per 16 x 16 tile of
+     * x (rows 16j.., columns 16c..) from the tile's amax instead of one per
+     * 1 x 16 block ([TE] timeline: "[Common] Enable NVFP4 2D block scaling in
+     * columnwise only"); the scale is stored for each of the tile's sixteen
+     * columnwise blocks, so the GEMM reads it as usual.  Round to nearest, no
+     * Hadamard transform (the weights' recipe); the rowwise direction keeps
+     * 1 x 16 blocks. */
+    NVQ_COL_2D = 4
 };
 
 /* nvq_nvfp4_quantize with flags (NVQ_AMAX_GIVEN or 0). */
@@ -203,8 +225,15 @@ NVQ_API nvq_status nvq_hybrid_quantize(const void* x, int64_t M, int64_t K, int6
                                const nvq_rht* rht_col, const nvq_sr* sr, nvq_qtensor* row,
                                nvq_qtensor* col, nvq_stream stream);
 
+/* nvq_hybrid_quantize with flags (NVQ_AMAX_GIVEN, NVQ_COL_2D). */
+NVQ_API nvq_status nvq_hybrid_quantize_ex(const void* x, int64_t M, int64_t K, int64_t ld, nvq_format row_fmt,
+                                          nvq_format col_fmt, int col_source, const nvq_rht* rht_col,
+                                          const nvq_sr* sr, int flags, nvq_qtensor* row, nvq_qtensor* col,
+                                          nvq_stream stream);
+
 /* Block-scaled GEMM, TN form: C[r][c] = alpha * sum_k A[r][k] B[c][k] + bias[c].
- * A, B: same format; A.cols == B.cols = K; A.rows = Mr and B.rows = Nc
+ * A, B: same format, or a row-scaled NVFP4 A with an NVFP4 B (alpha_r =
+ * (A.amax[r]/2688) * (B.amax[0]/2688)); A.cols == B.cols = K; A.rows = Mr and B.rows = Nc
  * multiples of 128 ([TT] every GEMM dim a multiple of 128); K a multiple of
  * 128.  alpha = (A.amax[0]/2688) * (B.amax[0]/2688) for NVFP4, 1 for MXFP8,
  * read on the device.  C: row-major [Mr][ldc], bf16 (c_fp32 = 0) or fp32
@@ -278,6 +307,44 @@ NVQ_API nvq_status nvq_nvfp4_linear_wgrad(const nvq_qtensor* dy_col, const nvq_q
                                   void* dw, nvq_stream stream);
 
 /* ------------------------------------------------------------------ */
+/* Linear layer with per-direction formats ([TE] Description: "MXFP8 fwd */
+/* and NVFP4 bwd (or vice versa)").  fwd_fmt, bwd_fmt: NVFP4 or MXFP8.    */
+/* The forward GEMM takes x and W rowwise in fwd_fmt; dgrad and wgrad take */
+/* the columnwise copies of W and x and both directions of dy in bwd_fmt, */
+/* all quantized from the original bf16.  An NVFP4 backward follows the   */
+/* NVFP4 recipe ([TT] "What changed"): the Hadamard transform on x's and  */
+/* dy's columnwise copies (the wgrad operands) and stochastic rounding on */
+/* dy.  M, N, K multiples of 128.                                         */
+/* ------------------------------------------------------------------ */
+enum {
+    /* W's NVFP4 columnwise copy (the dgrad operand) takes 16 x 16 2D
+     * scaling (NVQ_COL_2D). */
+    NVQ_W_COL_2D = 4
+};
+
+/* y[M][N] = x W^T (+ bias) in fwd_fmt; writes x_row, w_row ([M][K], [N][K]
+ * in fwd_fmt) and, when their data is non-NULL, saved_x_col ([K][M]) and
+ * saved_w_col ([K][N]) in bwd_fmt.  flags: NVQ_W_COL_2D or 0. */
+NVQ_API nvq_status nvq_hybrid_linear_fwd(const void* x, const void* w, const void* bias, int64_t M, int64_t N,
+                                         int64_t K, nvq_format fwd_fmt, nvq_format bwd_fmt, const nvq_rht* rht,
+                                         int flags, void* y, nvq_qtensor* x_row, nvq_qtensor* w_row,
+                                         nvq_qtensor* saved_x_col, nvq_qtensor* saved_w_col, nvq_stream stream);
+
+/* dy[M][N] -> dy_row [M][N] and dy_col [N][M] in bwd_fmt (NVFP4: sr on both,
+ * rht on dy_col; MXFP8: both ignored). */
+NVQ_API nvq_status nvq_hybrid_linear_bwd_quantize(const void* dy, int64_t M, int64_t N, nvq_format bwd_fmt,
+                                                  const nvq_rht* rht, const nvq_sr* sr, nvq_qtensor* dy_row,
+                                                  nvq_qtensor* dy_col, nvq_stream stream);
+
+/* dgrad dx[M][K] = TN(dy_row, saved_w_col) and wgrad dW[N][K] =
+ * TN(dy_col, saved_x_col) in whichever format the operands carry (both
+ * NVFP4 or both MXFP8), bf16. */
+NVQ_API nvq_status nvq_linear_dgrad(const nvq_qtensor* dy_row, const nvq_qtensor* saved_w_col, void* dx,
+                                    nvq_stream stream);
+NVQ_API nvq_status nvq_linear_wgrad(const nvq_qtensor* dy_col, const nvq_qtensor* saved_x_col, void* dw,
+                                    nvq_stream stream);
+
+/* ------------------------------------------------------------------ */
 /* Grouped (MoE) calls ([TE] GroupedLinear, _hybrid_split_quantize).    */
 /* Group g holds group_rows[g] >= 0 consecutive rows of the input        */
 /* (host array, G <= NVQ_MAX_GROUPS).  Quantized storage is padded per   */
@@ -333,6 +400,20 @@ NVQ_API nvq_status nvq_grouped_linear_fwd(const void* x, const void* w, const in
                                           int64_t N, int64_t K, void* y, nvq_qtensor* x_row,
                                           nvq_qtensor* w_row, nvq_qtensor* saved_x_col,
                                           nvq_qtensor* saved_w_col, nvq_stream stream);
+
+/* Flags of nvq_grouped_linear_fwd_ex. */
+enum {
+    /* The input's rowwise (forward) direction is row-scaled NVFP4 ([TE]
+     * Description: "row-scaled NVFP4 fwd + MXFP8 bwd"): x_row has format
+     * NVQ_FMT_NVFP4_ROWSCALED and P_G amaxes, one per padded row. */
+    NVQ_X_ROW_SCALED = 2
+};
+
+/* nvq_grouped_linear_fwd with flags (NVQ_X_ROW_SCALED or 0). */
+NVQ_API nvq_status nvq_grouped_linear_fwd_ex(const void* x, const void* w, const int64_t* group_rows, int G,
+                                             int64_t N, int64_t K, int flags, void* y, nvq_qtensor* x_row,
+                                             nvq_qtensor* w_row, nvq_qtensor* saved_x_col, nvq_qtensor* saved_w_col,
+                                             nvq_stream stream);
 
 /* dy bf16 [T][N] -> MXFP8 dy_row [P_G][N] and dy_col [N][P_G]. */
 NVQ_API nvq_status nvq_grouped_linear_bwd_quantize(const void* dy, const int64_t* group_rows, int G, int64_t N,

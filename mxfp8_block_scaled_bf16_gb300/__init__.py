@@ -22,7 +22,8 @@ import torch
 from . import build as _build
 
 __all__ = [
-    "NVFP4", "MXFP8", "IDENTITY", "NONE", "DIR_ROW", "DIR_COL", "AMAX_GIVEN", "COL_SOURCE_ORIGINAL",
+    "NVFP4", "MXFP8", "IDENTITY", "NVFP4_ROWSCALED", "X_ROW_SCALED", "COL_2D", "W_COL_2D", "NONE",
+    "hybrid_linear_fwd", "hybrid_linear_bwd_quantize", "linear_dgrad", "linear_wgrad", "DIR_ROW", "DIR_COL", "AMAX_GIVEN", "COL_SOURCE_ORIGINAL",
     "COL_SOURCE_ROWWISE_DEQUANTIZED", "NvqError", "QTensor", "lib", "load",
     "alloc_qtensor", "query_sizes", "colwise_cols", "amax", "nvfp4_quantize", "mxfp8_quantize",
     "hybrid_quantize", "gemm_tn", "nvfp4_linear_fwd", "nvfp4_linear_bwd_quantize",
@@ -32,7 +33,10 @@ __all__ = [
     "EXPORTED_SYMBOLS",
 ]
 
-NONE, NVFP4, MXFP8, IDENTITY = 0, 1, 2, 3
+NONE, NVFP4, MXFP8, IDENTITY, NVFP4_ROWSCALED = 0, 1, 2, 3, 4
+X_ROW_SCALED = 2
+COL_2D = 4
+W_COL_2D = 4
 COL_SOURCE_ORIGINAL, COL_SOURCE_ROWWISE_DEQUANTIZED = 0, 1
 DIR_ROW, DIR_COL = 1, 2
 AMAX_GIVEN = 1
@@ -74,6 +78,14 @@ _SIGS = {
     "nvq_nvfp4_quantize_ex": (_I32, [_P, _I64, _I64, _I64, _I32, ctypes.POINTER(_RHT), ctypes.POINTER(_SR), _I32, _QTP, _QTP, _P]),
     "nvq_mxfp8_quantize": (_I32, [_P, _I64, _I64, _I64, _I32, _QTP, _QTP, _P]),
     "nvq_hybrid_quantize": (_I32, [_P, _I64, _I64, _I64, _I32, _I32, _I32, ctypes.POINTER(_RHT), ctypes.POINTER(_SR), _QTP, _QTP, _P]),
+    "nvq_hybrid_quantize_ex": (_I32, [_P, _I64, _I64, _I64, _I32, _I32, _I32, ctypes.POINTER(_RHT), ctypes.POINTER(_SR),
+                                      _I32, _QTP, _QTP, _P]),
+    "nvq_hybrid_linear_fwd": (_I32, [_P, _P, _P, _I64, _I64, _I64, _I32, _I32, ctypes.POINTER(_RHT), _I32, _P, _QTP,
+                                     _QTP, _QTP, _QTP, _P]),
+    "nvq_hybrid_linear_bwd_quantize": (_I32, [_P, _I64, _I64, _I32, ctypes.POINTER(_RHT), ctypes.POINTER(_SR), _QTP,
+                                              _QTP, _P]),
+    "nvq_linear_dgrad": (_I32, [_QTP, _QTP, _P, _P]),
+    "nvq_linear_wgrad": (_I32, [_QTP, _QTP, _P, _P]),
     "nvq_gemm_tn": (_I32, [_QTP, _QTP, _P, _P, _I64, _I32, _P]),
     "nvq_gemm_tn_amax": (_I32, [_QTP, _QTP, _P, _P, _I64, _I32, ctypes.POINTER(_RHT), _P, _P, _P]),
     "nvq_nvfp4_linear_fwd": (_I32, [_P, _P, _P, _I64, _I64, _I64, ctypes.POINTER(_RHT), _P, _QTP, _QTP, _QTP, _QTP, _P]),
@@ -90,6 +102,8 @@ _SIGS = {
     "nvq_grouped_gemm_rows": (_I32, [_QTP, _QTP, ctypes.POINTER(_I64), _I32, _I64, _I32, _P, _I64, _P]),
     "nvq_grouped_gemm_wgrad": (_I32, [_QTP, _QTP, ctypes.POINTER(_I64), _I32, _P, _I64, _P]),
     "nvq_grouped_linear_fwd": (_I32, [_P, _P, ctypes.POINTER(_I64), _I32, _I64, _I64, _P, _QTP, _QTP, _QTP, _QTP, _P]),
+    "nvq_grouped_linear_fwd_ex": (_I32, [_P, _P, ctypes.POINTER(_I64), _I32, _I64, _I64, _I32, _P, _QTP, _QTP, _QTP,
+                                         _QTP, _P]),
     "nvq_grouped_linear_bwd_quantize": (_I32, [_P, ctypes.POINTER(_I64), _I32, _I64, _QTP, _QTP, _P]),
     "nvq_grouped_linear_dgrad": (_I32, [_QTP, _QTP, ctypes.POINTER(_I64), _I32, _P, _P]),
     "nvq_grouped_linear_wgrad": (_I32, [_QTP, _QTP, ctypes.POINTER(_I64), _I32, _P, _P]),
@@ -172,11 +186,16 @@ def colwise_cols(fmt: int, M: int) -> int:
     return load().nvq_colwise_cols(fmt, M)
 
 
-def alloc_qtensor(fmt: int, rows: int, cols: int, n_amax: int = 1, device="cuda") -> QTensor:
+def alloc_qtensor(fmt: int, rows: int, cols: int, n_amax: Optional[int] = None, device="cuda") -> QTensor:
+    """Storage for a [rows, cols] operand of `fmt`.  NVFP4 gets n_amax amaxes
+    (default 1; one per group for grouped storage), row-scaled NVFP4 one per row."""
     db, sb = query_sizes(fmt, rows, cols)
     data = torch.empty(max(db, 16), dtype=torch.uint8, device=device)
     scale = torch.empty(max(sb, 16), dtype=torch.uint8, device=device) if fmt != IDENTITY else None
-    amax = torch.empty(max(n_amax, 1), dtype=torch.float32, device=device) if fmt == NVFP4 else None
+    if n_amax is None:
+        n_amax = rows if fmt == NVFP4_ROWSCALED else 1
+    amax = (torch.empty(max(n_amax, 1), dtype=torch.float32, device=device)
+            if fmt in (NVFP4, NVFP4_ROWSCALED) else None)
     return QTensor(fmt, rows, cols, data, scale, amax)
 
 
@@ -214,7 +233,7 @@ def amax(x: torch.Tensor, rht_sign=None, stream=None):
 
 def hybrid_quantize(x: torch.Tensor, row_fmt: int, col_fmt: int, rht_sign=None, sr=None, stream=None,
                     out_row: Optional[QTensor] = None, out_col: Optional[QTensor] = None,
-                    col_source: int = COL_SOURCE_ORIGINAL):
+                    col_source: int = COL_SOURCE_ORIGINAL, col_2d: bool = False):
     """Rowwise in ``row_fmt`` and columnwise in ``col_fmt`` (NVFP4, MXFP8 or
     IDENTITY); the columnwise source is the original x or, with
     COL_SOURCE_ROWWISE_DEQUANTIZED, the dequantized rowwise value."""
@@ -222,14 +241,15 @@ def hybrid_quantize(x: torch.Tensor, row_fmt: int, col_fmt: int, rht_sign=None, 
     row = out_row or (alloc_qtensor(row_fmt, M, K, device=x.device) if row_fmt else None)
     col = out_col or (alloc_qtensor(col_fmt, K, colwise_cols(col_fmt, M), device=x.device) if col_fmt else None)
     rc, cc = (row.c() if row else None), (col.c() if col else None)
-    _check(load().nvq_hybrid_quantize(_ptr(x), M, K, ld, row_fmt, col_fmt, col_source, _rht(rht_sign), _sr(sr),
-                                      ctypes.byref(rc) if rc else None, ctypes.byref(cc) if cc else None,
-                                      _stream(stream)), "nvq_hybrid_quantize")
+    _check(load().nvq_hybrid_quantize_ex(_ptr(x), M, K, ld, row_fmt, col_fmt, col_source, _rht(rht_sign), _sr(sr),
+                                         COL_2D if col_2d else 0, ctypes.byref(rc) if rc else None,
+                                         ctypes.byref(cc) if cc else None, _stream(stream)), "nvq_hybrid_quantize_ex")
     return row, col
 
 
 def nvfp4_quantize(x: torch.Tensor, dirs: int = DIR_ROW | DIR_COL, rht_sign=None, sr=None, stream=None,
-                   out_row: Optional[QTensor] = None, out_col: Optional[QTensor] = None, amax_given: bool = False):
+                   out_row: Optional[QTensor] = None, out_col: Optional[QTensor] = None, amax_given: bool = False,
+                   col_2d: bool = False):
     """NVFP4 row and/or column quantization.  amax_given: the outputs' amax
     buffers already hold x's amaxes (written by the GEMM that produced x), so
     the amax pass is skipped."""
@@ -237,7 +257,8 @@ def nvfp4_quantize(x: torch.Tensor, dirs: int = DIR_ROW | DIR_COL, rht_sign=None
     row = out_row or (alloc_qtensor(NVFP4, M, K, device=x.device) if dirs & DIR_ROW else None)
     col = out_col or (alloc_qtensor(NVFP4, K, colwise_cols(NVFP4, M), device=x.device) if dirs & DIR_COL else None)
     rc, cc = (row.c() if row else None), (col.c() if col else None)
-    _check(load().nvq_nvfp4_quantize_ex(_ptr(x), M, K, ld, dirs, _rht(rht_sign), _sr(sr), AMAX_GIVEN if amax_given else 0,
+    flags = (AMAX_GIVEN if amax_given else 0) | (COL_2D if col_2d else 0)
+    _check(load().nvq_nvfp4_quantize_ex(_ptr(x), M, K, ld, dirs, _rht(rht_sign), _sr(sr), flags,
                                         ctypes.byref(rc) if rc else None, ctypes.byref(cc) if cc else None,
                                         _stream(stream)), "nvq_nvfp4_quantize_ex")
     return row, col
@@ -333,6 +354,55 @@ def nvfp4_linear_wgrad(dy_col: QTensor, x_col: QTensor, dw: Optional[torch.Tenso
     return dw
 
 
+def hybrid_linear_fwd(x: torch.Tensor, w: torch.Tensor, fwd_fmt: int, bwd_fmt: int, bias=None, rht_sign=None,
+                      w_col_2d: bool = False, save_for_backward=True, stream=None, y: Optional[torch.Tensor] = None,
+                      bufs=None):
+    """Linear forward with per-direction formats (e.g. MXFP8 forward, NVFP4
+    backward): y = x W^T in fwd_fmt; saved x_col / w_col in bwd_fmt."""
+    M, K, _ = _bf16_2d(x)
+    N = w.shape[0]
+    if bufs is None:
+        bufs = dict(x_row=alloc_qtensor(fwd_fmt, M, K, device=x.device), w_row=alloc_qtensor(fwd_fmt, N, K, device=x.device),
+                    x_col=alloc_qtensor(bwd_fmt, K, colwise_cols(bwd_fmt, M), device=x.device) if save_for_backward else None,
+                    w_col=alloc_qtensor(bwd_fmt, K, colwise_cols(bwd_fmt, N), device=x.device) if save_for_backward else None)
+    if y is None:
+        y = torch.empty(M, N, dtype=torch.bfloat16, device=x.device)
+    xr, wr = bufs["x_row"].c(), bufs["w_row"].c()
+    xc = bufs["x_col"].c() if bufs.get("x_col") is not None else _QT()
+    wc = bufs["w_col"].c() if bufs.get("w_col") is not None else _QT()
+    _check(load().nvq_hybrid_linear_fwd(_ptr(x), _ptr(w), _ptr(bias), M, N, K, fwd_fmt, bwd_fmt, _rht(rht_sign),
+                                        W_COL_2D if w_col_2d else 0, _ptr(y), ctypes.byref(xr), ctypes.byref(wr),
+                                        ctypes.byref(xc), ctypes.byref(wc), _stream(stream)), "nvq_hybrid_linear_fwd")
+    return y, bufs
+
+
+def hybrid_linear_bwd_quantize(dy: torch.Tensor, bwd_fmt: int, rht_sign=None, sr=None, stream=None, bufs=None):
+    M, N, _ = _bf16_2d(dy)
+    if bufs is None:
+        bufs = dict(dy_row=alloc_qtensor(bwd_fmt, M, N, device=dy.device),
+                    dy_col=alloc_qtensor(bwd_fmt, N, colwise_cols(bwd_fmt, M), device=dy.device))
+    r, c = bufs["dy_row"].c(), bufs["dy_col"].c()
+    _check(load().nvq_hybrid_linear_bwd_quantize(_ptr(dy), M, N, bwd_fmt, _rht(rht_sign), _sr(sr), ctypes.byref(r),
+                                                 ctypes.byref(c), _stream(stream)), "nvq_hybrid_linear_bwd_quantize")
+    return bufs
+
+
+def linear_dgrad(dy_row: QTensor, w_col: QTensor, dx: Optional[torch.Tensor] = None, stream=None):
+    if dx is None:
+        dx = torch.empty(dy_row.rows, w_col.rows, dtype=torch.bfloat16, device=dy_row.data.device)
+    a, b = dy_row.c(), w_col.c()
+    _check(load().nvq_linear_dgrad(ctypes.byref(a), ctypes.byref(b), _ptr(dx), _stream(stream)), "nvq_linear_dgrad")
+    return dx
+
+
+def linear_wgrad(dy_col: QTensor, x_col: QTensor, dw: Optional[torch.Tensor] = None, stream=None):
+    if dw is None:
+        dw = torch.empty(dy_col.rows, x_col.rows, dtype=torch.bfloat16, device=dy_col.data.device)
+    a, b = dy_col.c(), x_col.c()
+    _check(load().nvq_linear_wgrad(ctypes.byref(a), ctypes.byref(b), _ptr(dw), _stream(stream)), "nvq_linear_wgrad")
+    return dw
+
+
 def _groups(group_rows: Sequence[int]):
     g = [int(v) for v in group_rows]
     return (_I64 * len(g))(*g), len(g)
@@ -349,7 +419,8 @@ def grouped_hybrid_quantize(x: torch.Tensor, group_rows: Sequence[int], row_fmt:
     M, K, ld = _bf16_2d(x)
     arr, G = _groups(group_rows)
     P = load().nvq_grouped_padded_rows(arr, G)
-    row = out_row or (alloc_qtensor(row_fmt, P, K, n_amax=G, device=x.device) if row_fmt else None)
+    row = out_row or (alloc_qtensor(row_fmt, P, K, n_amax=P if row_fmt == NVFP4_ROWSCALED else G, device=x.device)
+                      if row_fmt else None)
     col = out_col or (alloc_qtensor(col_fmt, K, P, n_amax=G, device=x.device) if col_fmt else None)
     rc, cc = (row.c() if row else None), (col.c() if col else None)
     _check(load().nvq_grouped_hybrid_quantize(_ptr(x), K, ld, arr, G, row_fmt, col_fmt,
@@ -383,17 +454,19 @@ def grouped_gemm_wgrad(A: QTensor, B: QTensor, group_rows: Sequence[int], out: O
 
 
 def grouped_linear_fwd(x: torch.Tensor, w: torch.Tensor, group_rows: Sequence[int], stream=None,
-                       y: Optional[torch.Tensor] = None, bufs=None, save_for_backward=True):
+                       y: Optional[torch.Tensor] = None, bufs=None, save_for_backward=True, row_scaled_x: bool = False):
     """Grouped (MoE) linear forward, NVFP4: x [T][K], w [G][N][K] or [G*N][K];
     returns (y [T][N], bufs) with bufs holding x_row, w_row and, for the
-    backward, MXFP8 x_col and w_col."""
+    backward, MXFP8 x_col and w_col.  row_scaled_x: x's rowwise direction is
+    row-scaled NVFP4 (one FP32 outer scale per row)."""
     T, K, _ = _bf16_2d(x)
     arr, G = _groups(group_rows)
     w2 = w.reshape(-1, w.shape[-1])
     N = w2.shape[0] // G
     P = load().nvq_grouped_padded_rows(arr, G)
     if bufs is None:
-        bufs = dict(x_row=alloc_qtensor(NVFP4, P, K, n_amax=G, device=x.device),
+        bufs = dict(x_row=(alloc_qtensor(NVFP4_ROWSCALED, P, K, device=x.device) if row_scaled_x
+                           else alloc_qtensor(NVFP4, P, K, n_amax=G, device=x.device)),
                     w_row=alloc_qtensor(NVFP4, G * N, K, n_amax=G, device=x.device),
                     x_col=alloc_qtensor(MXFP8, K, P, device=x.device) if save_for_backward else None,
                     w_col=alloc_qtensor(MXFP8, K, G * N, device=x.device) if save_for_backward else None)
@@ -402,8 +475,9 @@ def grouped_linear_fwd(x: torch.Tensor, w: torch.Tensor, group_rows: Sequence[in
     xr, wr = bufs["x_row"].c(), bufs["w_row"].c()
     xc = bufs["x_col"].c() if bufs.get("x_col") is not None else _QT()
     wc = bufs["w_col"].c() if bufs.get("w_col") is not None else _QT()
-    _check(load().nvq_grouped_linear_fwd(_ptr(x), _ptr(w2), arr, G, N, K, _ptr(y), ctypes.byref(xr), ctypes.byref(wr),
-                                         ctypes.byref(xc), ctypes.byref(wc), _stream(stream)), "nvq_grouped_linear_fwd")
+    _check(load().nvq_grouped_linear_fwd_ex(_ptr(x), _ptr(w2), arr, G, N, K, X_ROW_SCALED if row_scaled_x else 0,
+                                            _ptr(y), ctypes.byref(xr), ctypes.byref(wr), ctypes.byref(xc),
+                                            ctypes.byref(wc), _stream(stream)), "nvq_grouped_linear_fwd_ex")
     return y, bufs
 
 

@@ -112,11 +112,12 @@ inline int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
 // columnwise storage to 16 like NVFP4 and has no scales
 inline int block_of(nvq_format f) { return f == NVQ_FMT_MXFP8 ? 32 : 16; }
 inline bool valid_fmt(nvq_format f) { return f == NVQ_FMT_NVFP4 || f == NVQ_FMT_MXFP8; }
-inline bool valid_qfmt(nvq_format f) { return valid_fmt(f) || f == NVQ_FMT_IDENTITY; }
+inline bool valid_qfmt(nvq_format f) { return valid_fmt(f) || f == NVQ_FMT_IDENTITY || f == NVQ_FMT_NVFP4_ROWSCALED; }
+inline bool is_nvfp4(nvq_format f) { return f == NVQ_FMT_NVFP4 || f == NVQ_FMT_NVFP4_ROWSCALED; }
 
 int64_t data_bytes(nvq_format f, int64_t rows, int64_t cols)
 {
-    return f == NVQ_FMT_NVFP4 ? rows * (cols / 2) : f == NVQ_FMT_IDENTITY ? rows * cols * 2 : rows * cols;
+    return is_nvfp4(f) ? rows * (cols / 2) : f == NVQ_FMT_IDENTITY ? rows * cols * 2 : rows * cols;
 }
 
 int64_t scale_ctiles(nvq_format f, int64_t cols) { return ceil_div(cols / block_of(f), 4); }
@@ -125,10 +126,10 @@ nvq_status check_qtensor(const nvq_qtensor* t, nvq_format fmt, int64_t rows, int
 {
     if (!t || !t->data || (!t->scale && fmt != NVQ_FMT_IDENTITY)) return NVQ_ERR_NULL;
     if (t->fmt != fmt) return NVQ_ERR_UNSUPPORTED;
-    if (fmt == NVQ_FMT_NVFP4 && !t->amax) return NVQ_ERR_NULL;
+    if (is_nvfp4(fmt) && !t->amax) return NVQ_ERR_NULL;
     if (t->rows != rows || t->cols != cols) return NVQ_ERR_SHAPE;
     if (!aligned16(t->data) || (fmt != NVQ_FMT_IDENTITY && !aligned16(t->scale)) ||
-        (fmt == NVQ_FMT_NVFP4 && (reinterpret_cast<uintptr_t>(t->amax) & 3)))
+        (is_nvfp4(fmt) && (reinterpret_cast<uintptr_t>(t->amax) & 3)))
         return NVQ_ERR_ALIGN;
     return NVQ_OK;
 }
@@ -151,7 +152,7 @@ uint32_t sign_mask(const nvq_rht* rht, bool* ok)
 nvq_status quantize_impl(const void* x, int64_t M, int64_t K, int64_t ld, const int64_t* group_rows, int G,
                          nvq_format row_fmt, nvq_format col_fmt, const nvq_rht* rht_col, const nvq_sr* sr,
                          nvq_qtensor* row, nvq_qtensor* col, cudaStream_t stream, bool amax_given = false,
-                         int col_source = NVQ_COL_SOURCE_ORIGINAL)
+                         int col_source = NVQ_COL_SOURCE_ORIGINAL, bool col_2d = false)
 {
     if (row_fmt != NVQ_FMT_NONE && !valid_qfmt(row_fmt)) return NVQ_ERR_UNSUPPORTED;
     if (col_fmt != NVQ_FMT_NONE && !valid_qfmt(col_fmt)) return NVQ_ERR_UNSUPPORTED;
@@ -159,8 +160,17 @@ nvq_status quantize_impl(const void* x, int64_t M, int64_t K, int64_t ld, const 
     if (col_source != NVQ_COL_SOURCE_ORIGINAL && !dq) return NVQ_ERR_UNSUPPORTED;
     // the rowwise-dequantized source needs a quantized rowwise direction
     if (dq && (!valid_fmt(row_fmt) || col_fmt == NVQ_FMT_NONE)) return NVQ_ERR_UNSUPPORTED;
-    const bool hybrid_kernel = dq || row_fmt == NVQ_FMT_IDENTITY || col_fmt == NVQ_FMT_IDENTITY;
-    if (hybrid_kernel && group_rows) return NVQ_ERR_UNSUPPORTED;
+    // row-scaled NVFP4 is a rowwise format, with an MXFP8 columnwise direction or none
+    if (col_fmt == NVQ_FMT_NVFP4_ROWSCALED) return NVQ_ERR_UNSUPPORTED;
+    const bool row_scaled = row_fmt == NVQ_FMT_NVFP4_ROWSCALED;
+    if (row_scaled && (dq || (col_fmt != NVQ_FMT_NONE && col_fmt != NVQ_FMT_MXFP8))) return NVQ_ERR_UNSUPPORTED;
+    // 16 x 16 (2D) scaling of an NVFP4 columnwise direction, round to nearest
+    // (the weights' recipe: no Hadamard transform, no stochastic rounding)
+    if (col_2d && (col_fmt != NVQ_FMT_NVFP4 || rht_col || sr || dq || row_scaled || row_fmt == NVQ_FMT_IDENTITY))
+        return NVQ_ERR_UNSUPPORTED;
+    const bool hybrid_kernel =
+        dq || row_scaled || col_2d || row_fmt == NVQ_FMT_IDENTITY || col_fmt == NVQ_FMT_IDENTITY;
+    if (hybrid_kernel && !row_scaled && group_rows) return NVQ_ERR_UNSUPPORTED;
     if (K < 0 || ld < K || (ld % 8) != 0) return NVQ_ERR_SHAPE;
     if (!aligned16(x)) return NVQ_ERR_ALIGN;
     if ((row_fmt != NVQ_FMT_NONE && K % block_of(row_fmt)) || K % 16) return NVQ_ERR_SHAPE;
@@ -251,6 +261,8 @@ nvq_status quantize_impl(const void* x, int64_t M, int64_t K, int64_t ld, const 
         // nothing to read: zero the outputs that exist (scales / amax)
         cudaError_t e = cudaSuccess;
         if (do_row && row_fmt == NVQ_FMT_NVFP4) e = cudaMemsetAsync(row->amax, 0, sizeof(float) * nG, stream);
+        if (e == cudaSuccess && do_row && row_scaled && row_rows > 0)
+            e = cudaMemsetAsync(row->amax, 0, sizeof(float) * row_rows, stream);
         if (e == cudaSuccess && do_col && col_fmt == NVQ_FMT_NVFP4)
             e = cudaMemsetAsync(col->amax, 0, sizeof(float) * nG, stream);
         if (e == cudaSuccess && do_col && K > 0) {
@@ -282,6 +294,8 @@ nvq_status quantize_impl(const void* x, int64_t M, int64_t K, int64_t ld, const 
     }
     if (!hybrid_kernel)
         return cuda_status(launch_quantize(a, (int)row_fmt, (int)col_fmt, rht, sr != nullptr, row_tiles, stream));
+    if (row_scaled && !amax_given && launch_row_amax(a, row_rows, row->amax, stream) != cudaSuccess)
+        return NVQ_ERR_CUDA;
     if (dq && col_fmt == NVQ_FMT_NVFP4) {
         // The columnwise scale needs the amax of the dequantized values before
         // any block is quantized: a first pass writes the rowwise operand and
@@ -296,7 +310,8 @@ nvq_status quantize_impl(const void* x, int64_t M, int64_t K, int64_t ld, const 
             return NVQ_ERR_CUDA;
         a.row_data = nullptr;
     }
-    return cuda_status(launch_quantize_hybrid(a, (int)row_fmt, (int)col_fmt, rht, sr != nullptr, dq, row_tiles, stream));
+    const int col_code = col_2d ? 5 : (int)col_fmt;  // 5: the kernel's tile-scaled NVFP4 columnwise format
+    return cuda_status(launch_quantize_hybrid(a, (int)row_fmt, col_code, rht, sr != nullptr, dq, row_tiles, stream));
 }
 
 // Test hook for the bounded waits: with NVQ_DEBUG_DROP_TMA=1 in the
@@ -315,12 +330,21 @@ bool debug_drop_this_launch()
     return on && !used.exchange(true);
 }
 
+// Operand formats a GEMM takes: both NVFP4, both MXFP8, or a row-scaled NVFP4
+// A with an NVFP4 B (the per-row outer scale of A goes into the epilogue's
+// alpha).
+bool gemm_formats_ok(const nvq_qtensor* A, const nvq_qtensor* B)
+{
+    if (A->fmt == NVQ_FMT_NVFP4_ROWSCALED) return B->fmt == NVQ_FMT_NVFP4;
+    return A->fmt == B->fmt && valid_fmt(A->fmt);
+}
+
 nvq_status gemm_prepare(const nvq_qtensor* A, const nvq_qtensor* B, int64_t n_out, CUtensorMap* am, CUtensorMap* bm,
                         GemmArgs* g)
 {
     if (!A || !B || !A->data || !B->data || !A->scale || !B->scale) return NVQ_ERR_NULL;
-    if (A->fmt != B->fmt || !valid_fmt(A->fmt)) return NVQ_ERR_UNSUPPORTED;
-    const nvq_format f = A->fmt;
+    if (!gemm_formats_ok(A, B)) return NVQ_ERR_UNSUPPORTED;
+    const nvq_format f = B->fmt;  // the tensor-core format (a row-scaled A is NVFP4 on the tensor core)
     if (f == NVQ_FMT_NVFP4 && (!A->amax || !B->amax)) return NVQ_ERR_NULL;
     if (A->rows < 0 || B->rows < 0 || A->cols < 0 || A->rows % 128 || B->rows % 128) return NVQ_ERR_SHAPE;
     if (A->cols % 128 || B->cols % 128) return NVQ_ERR_SHAPE;
@@ -338,6 +362,7 @@ nvq_status gemm_prepare(const nvq_qtensor* A, const nvq_qtensor* B, int64_t n_ou
     g->b_scale_ctiles = scale_ctiles(f, B->cols);
     g->a_amax = A->amax;
     g->b_amax = B->amax;
+    g->a_row_scaled = A->fmt == NVQ_FMT_NVFP4_ROWSCALED ? 1 : 0;
     if (n_out % 128) return NVQ_ERR_SHAPE;
     g->block_n = gemm_block_n(n_out);
     int* status = nullptr;
@@ -417,7 +442,7 @@ nvq_status gemm_tn_impl(const nvq_qtensor* A, const nvq_qtensor* B, const void* 
                         int c_fp32, const nvq_rht* rht, float* c_amax, float* c_amax_rht, cudaStream_t stream)
 {
     if (!A || !B) return NVQ_ERR_NULL;
-    if (A->fmt == B->fmt && A->cols != B->cols) return NVQ_ERR_SHAPE;
+    if (gemm_formats_ok(A, B) && A->cols != B->cols) return NVQ_ERR_SHAPE;
     if ((c_amax && (reinterpret_cast<uintptr_t>(c_amax) & 3)) || (c_amax_rht && (reinterpret_cast<uintptr_t>(c_amax_rht) & 3)))
         return NVQ_ERR_ALIGN;
     uint32_t mask = 0;
@@ -539,6 +564,61 @@ nvq_status nvq_hybrid_quantize(const void* x, int64_t M, int64_t K, int64_t ld, 
                          reinterpret_cast<cudaStream_t>(stream), false, col_source);
 }
 
+nvq_status nvq_hybrid_quantize_ex(const void* x, int64_t M, int64_t K, int64_t ld, nvq_format row_fmt,
+                                  nvq_format col_fmt, int col_source, const nvq_rht* rht_col, const nvq_sr* sr,
+                                  int flags, nvq_qtensor* row, nvq_qtensor* col, nvq_stream stream)
+{
+    if (flags & ~(NVQ_AMAX_GIVEN | NVQ_COL_2D)) return NVQ_ERR_UNSUPPORTED;
+    return quantize_impl(x, M, K, ld, nullptr, 1, row_fmt, col_fmt, rht_col, sr, row, col,
+                         reinterpret_cast<cudaStream_t>(stream), (flags & NVQ_AMAX_GIVEN) != 0, col_source,
+                         (flags & NVQ_COL_2D) != 0);
+}
+
+nvq_status nvq_hybrid_linear_fwd(const void* x, const void* w, const void* bias, int64_t M, int64_t N, int64_t K,
+                                 nvq_format fwd_fmt, nvq_format bwd_fmt, const nvq_rht* rht, int flags, void* y,
+                                 nvq_qtensor* x_row, nvq_qtensor* w_row, nvq_qtensor* saved_x_col,
+                                 nvq_qtensor* saved_w_col, nvq_stream stream)
+{
+    if (!x || !w || !y || !x_row || !w_row) return NVQ_ERR_NULL;
+    if (M % 128 || N % 128 || K % 128 || M <= 0 || N <= 0 || K <= 0) return NVQ_ERR_SHAPE;
+    if (!valid_fmt(fwd_fmt) || !valid_fmt(bwd_fmt)) return NVQ_ERR_UNSUPPORTED;
+    if (flags & ~NVQ_W_COL_2D) return NVQ_ERR_UNSUPPORTED;
+    const bool nv_bwd = bwd_fmt == NVQ_FMT_NVFP4;
+    if ((flags & NVQ_W_COL_2D) && !nv_bwd) return NVQ_ERR_UNSUPPORTED;
+    const bool xc = saved_x_col && saved_x_col->data, wc = saved_w_col && saved_w_col->data;
+    nvq_status s = nvq_hybrid_quantize_ex(x, M, K, K, fwd_fmt, xc ? bwd_fmt : NVQ_FMT_NONE, NVQ_COL_SOURCE_ORIGINAL,
+                                          nv_bwd ? rht : nullptr, nullptr, 0, x_row, xc ? saved_x_col : nullptr, stream);
+    if (s != NVQ_OK) return s;
+    s = nvq_hybrid_quantize_ex(w, N, K, K, fwd_fmt, wc ? bwd_fmt : NVQ_FMT_NONE, NVQ_COL_SOURCE_ORIGINAL, nullptr,
+                               nullptr, (wc && (flags & NVQ_W_COL_2D)) ? NVQ_COL_2D : 0, w_row,
+                               wc ? saved_w_col : nullptr, stream);
+    if (s != NVQ_OK) return s;
+    return nvq_gemm_tn(x_row, w_row, bias, y, N, 0, stream);
+}
+
+nvq_status nvq_hybrid_linear_bwd_quantize(const void* dy, int64_t M, int64_t N, nvq_format bwd_fmt,
+                                          const nvq_rht* rht, const nvq_sr* sr, nvq_qtensor* dy_row,
+                                          nvq_qtensor* dy_col, nvq_stream stream)
+{
+    if (M % 128 || N % 128) return NVQ_ERR_SHAPE;
+    if (!valid_fmt(bwd_fmt)) return NVQ_ERR_UNSUPPORTED;
+    const bool nv = bwd_fmt == NVQ_FMT_NVFP4;
+    return nvq_hybrid_quantize(dy, M, N, N, bwd_fmt, bwd_fmt, NVQ_COL_SOURCE_ORIGINAL, nv ? rht : nullptr,
+                               nv ? sr : nullptr, dy_row, dy_col, stream);
+}
+
+nvq_status nvq_linear_dgrad(const nvq_qtensor* dy_row, const nvq_qtensor* saved_w_col, void* dx, nvq_stream stream)
+{
+    if (!dy_row || !saved_w_col) return NVQ_ERR_NULL;
+    return nvq_gemm_tn(dy_row, saved_w_col, nullptr, dx, saved_w_col->rows, 0, stream);
+}
+
+nvq_status nvq_linear_wgrad(const nvq_qtensor* dy_col, const nvq_qtensor* saved_x_col, void* dw, nvq_stream stream)
+{
+    if (!dy_col || !saved_x_col) return NVQ_ERR_NULL;
+    return nvq_gemm_tn(dy_col, saved_x_col, nullptr, dw, saved_x_col->rows, 0, stream);
+}
+
 nvq_status nvq_gemm_tn(const nvq_qtensor* A, const nvq_qtensor* B, const void* bias, void* C, int64_t ldc,
                        int c_fp32, nvq_stream stream)
 {
@@ -556,10 +636,11 @@ nvq_status nvq_nvfp4_quantize_ex(const void* x, int64_t M, int64_t K, int64_t ld
                                  const nvq_sr* sr, int flags, nvq_qtensor* row, nvq_qtensor* col, nvq_stream stream)
 {
     if (dirs & ~(NVQ_DIR_ROW | NVQ_DIR_COL)) return NVQ_ERR_UNSUPPORTED;
-    if (flags & ~NVQ_AMAX_GIVEN) return NVQ_ERR_UNSUPPORTED;
+    if (flags & ~(NVQ_AMAX_GIVEN | NVQ_COL_2D)) return NVQ_ERR_UNSUPPORTED;
     return quantize_impl(x, M, K, ld, nullptr, 1, (dirs & NVQ_DIR_ROW) ? NVQ_FMT_NVFP4 : NVQ_FMT_NONE,
                          (dirs & NVQ_DIR_COL) ? NVQ_FMT_NVFP4 : NVQ_FMT_NONE, rht_col, sr, row, col,
-                         reinterpret_cast<cudaStream_t>(stream), (flags & NVQ_AMAX_GIVEN) != 0);
+                         reinterpret_cast<cudaStream_t>(stream), (flags & NVQ_AMAX_GIVEN) != 0,
+                         NVQ_COL_SOURCE_ORIGINAL, (flags & NVQ_COL_2D) != 0);
 }
 nvq_status nvq_nvfp4_linear_fwd_ex(const void* x, const void* w, const void* bias, int64_t M, int64_t N, int64_t K,
                                    const nvq_rht* rht, int flags, void* y, float* y_amax, float* y_amax_rht,
@@ -659,7 +740,8 @@ nvq_status nvq_grouped_gemm_rows(const nvq_qtensor* A, const nvq_qtensor* B, con
         return NVQ_ERR_NULL;
     }
     const int64_t n_out_guess = b_col_groups ? B->rows : n_per_group;
-    nvq_status s = gemm_prepare(A, B, n_out_guess, &am, &bm, g);
+    nvq_status s = (b_col_groups && A->fmt == NVQ_FMT_NVFP4_ROWSCALED) ? NVQ_ERR_UNSUPPORTED
+                                                                      : gemm_prepare(A, B, n_out_guess, &am, &bm, g);
     int64_t n_out = 0, klen = 0;
     if (s == NVQ_OK) {
         if (n_per_group <= 0 || n_per_group % 128) s = NVQ_ERR_SHAPE;
@@ -717,7 +799,7 @@ nvq_status nvq_grouped_gemm_wgrad(const nvq_qtensor* A, const nvq_qtensor* B, co
         delete g;
         return NVQ_ERR_NULL;
     }
-    nvq_status s = gemm_prepare(A, B, B->rows, &am, &bm, g);
+    nvq_status s = A->fmt == NVQ_FMT_NVFP4_ROWSCALED ? NVQ_ERR_UNSUPPORTED : gemm_prepare(A, B, B->rows, &am, &bm, g);
     if (s == NVQ_OK && (A->cols != B->cols || nvq_grouped_padded_rows(group_rows, G) != A->cols)) s = NVQ_ERR_SHAPE;
     if (s == NVQ_OK) s = check_c(C, ldc, B->rows, 0);
     if (s == NVQ_OK) {
@@ -753,10 +835,19 @@ nvq_status nvq_grouped_linear_fwd(const void* x, const void* w, const int64_t* g
                                   int64_t K, void* y, nvq_qtensor* x_row, nvq_qtensor* w_row,
                                   nvq_qtensor* saved_x_col, nvq_qtensor* saved_w_col, nvq_stream stream)
 {
+    return nvq_grouped_linear_fwd_ex(x, w, group_rows, G, N, K, 0, y, x_row, w_row, saved_x_col, saved_w_col, stream);
+}
+
+nvq_status nvq_grouped_linear_fwd_ex(const void* x, const void* w, const int64_t* group_rows, int G, int64_t N,
+                                     int64_t K, int flags, void* y, nvq_qtensor* x_row, nvq_qtensor* w_row,
+                                     nvq_qtensor* saved_x_col, nvq_qtensor* saved_w_col, nvq_stream stream)
+{
     if (!group_rows || !x_row || !w_row || !y) return NVQ_ERR_NULL;
     if (G < 1 || G > kMaxGroups || N <= 0 || K <= 0) return NVQ_ERR_SHAPE;
+    if (flags & ~NVQ_X_ROW_SCALED) return NVQ_ERR_UNSUPPORTED;
     const bool xc = saved_x_col && saved_x_col->data, wc = saved_w_col && saved_w_col->data;
-    nvq_status s = nvq_grouped_hybrid_quantize(x, K, K, group_rows, G, NVQ_FMT_NVFP4,
+    const nvq_format xf = (flags & NVQ_X_ROW_SCALED) ? NVQ_FMT_NVFP4_ROWSCALED : NVQ_FMT_NVFP4;
+    nvq_status s = nvq_grouped_hybrid_quantize(x, K, K, group_rows, G, xf,
                                                xc ? NVQ_FMT_MXFP8 : NVQ_FMT_NONE, x_row, xc ? saved_x_col : nullptr,
                                                nullptr, nullptr, stream);
     if (s != NVQ_OK) return s;

@@ -388,7 +388,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool row_ok = out_row < gr.rows_valid;
             float alpha = 1.0f;
             if (FMT == 1) {
-                const float ga = __fdiv_rn(args.a_amax[gr.amax_idx], 2688.0f);
+                // row-scaled A: this lane's row's own outer scale (rows past the group's are not stored)
+                const float aa = !args.a_row_scaled ? args.a_amax[gr.amax_idx]
+                                 : row_ok ? args.a_amax[gr.a_row0 + out_row] : 0.0f;
+                const float ga = __fdiv_rn(aa, 2688.0f);
                 const float gb = __fdiv_rn(args.b_amax[gr.amax_idx], 2688.0f);
                 alpha = __fmul_rn(ga, gb);
             }

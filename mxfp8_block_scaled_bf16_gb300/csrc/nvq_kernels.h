@@ -58,6 +58,8 @@ cudaError_t launch_quantize(const QuantArgs& a, int row_fmt, int col_fmt, bool r
 // columnwise source (dq): quantize_hybrid.cu.
 cudaError_t launch_quantize_hybrid(const QuantArgs& a, int row_fmt, int col_fmt, bool rht, bool sr, bool dq,
                                    int64_t row_tiles, cudaStream_t s);
+// Per-row amax of the padded row space (row-scaled NVFP4): amax_rows[n_rows].
+cudaError_t launch_row_amax(const QuantArgs& a, int64_t n_rows, float* amax_rows, cudaStream_t s);
 
 // ------------------------------------------------------------------ GEMM
 // One GEMM problem (or one group of a grouped GEMM) in TN form.
@@ -91,6 +93,7 @@ struct GemmArgs {
     int64_t b_scale_ctiles;
     const float* a_amax;
     const float* b_amax;
+    int a_row_scaled;  // A is row-scaled NVFP4: a_amax holds one amax per (padded) row of A
     const uint16_t* bias;  // bf16 [N] or NULL
     void* C;
     int64_t ldc;

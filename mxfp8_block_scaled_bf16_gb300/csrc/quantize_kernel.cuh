@@ -274,7 +274,7 @@ __device__ __noinline__ void nvfp4_fill_q_tab(const QuantArgs& a, int g, float (
         const int dir = threadIdx.x >> 4, n = threadIdx.x & 15;
         float A = 0.0f;
         if (dir == 0 && ROW_FMT == 1) A = a.row_amax[g];
-        if (dir == 1 && COL_FMT == 1) A = a.col_amax[g];
+        if (dir == 1 && (COL_FMT == 1 || COL_FMT == 5)) A = a.col_amax[g];
         const Nvfp4Scale ts = nvfp4_tensor_scale(A);
         q_tab[dir][n] = n ? __fdiv_rn(ts.s_enc, (float)n) : 0.0f;
     }
@@ -381,7 +381,11 @@ struct QuantSmem {
 __device__ __forceinline__ int col_chunk_nv(int kk, int ch8) { return kk * 64 + ((ch8 ^ ((kk >> 3) & 7)) << 3); }
 __device__ __forceinline__ int col_chunk_mx(int kk, int ch16) { return kk * 128 + ((ch16 ^ ((kk >> 3) & 7)) << 4); }
 
-// Formats: 0 none, 1 NVFP4, 2 MXFP8, 3 identity (bf16).  DQ: the columnwise
+// Formats: 0 none, 1 NVFP4, 2 MXFP8, 3 identity (bf16), 4 row-scaled NVFP4
+// (rowwise only: row p's FP32 outer scale from its own amax row_amax[p]), 5
+// NVFP4 with one scale per 16 x 16 tile (columnwise only: the tile's amax,
+// the thread's 16 x 8 half and its lane partner's, sets the scale of all its
+// 1 x 16 columnwise blocks).  DQ: the columnwise
 // direction quantizes the dequantized rowwise values (the tile is replaced by
 // them after the rowwise pass).  Run-time modes (CTA-uniform): row_data ==
 // NULL skips the rowwise stores; col_data == NULL skips the columnwise pass;
@@ -412,7 +416,7 @@ __global__ void __launch_bounds__(kThreads, 2) quantize_kernel(QuantArgs a)
 
     constexpr bool kRowTab = !(ROW_FMT == 1 && COL_FMT == 2);
     __shared__ float q_tab[2][16];
-    if constexpr ((ROW_FMT == 1 && kRowTab) || COL_FMT == 1) nvfp4_fill_q_tab<ROW_FMT, COL_FMT>(a, g, q_tab);
+    if constexpr ((ROW_FMT == 1 && kRowTab) || COL_FMT == 1 || COL_FMT == 5) nvfp4_fill_q_tab<ROW_FMT, COL_FMT>(a, g, q_tab);
     __shared__ float e2m1_tab[16];  // signed E2M1 values by code (rowwise-dequantized NVFP4)
     if constexpr (DQ && ROW_FMT == 1) {
         if (threadIdx.x < 16) {
@@ -427,8 +431,9 @@ __global__ void __launch_bounds__(kThreads, 2) quantize_kernel(QuantArgs a)
     __syncthreads();  // staging cleared, q_tab filled
 
     // ---------------- rowwise direction
-    if constexpr (ROW_FMT == 1) {  // NVFP4, 16-blocks = lane pair
-        const Nvfp4Scale ts = nvfp4_tensor_scale(a.row_amax[g]);
+    if constexpr (ROW_FMT == 1 || ROW_FMT == 4) {  // NVFP4, 16-blocks = lane pair
+        constexpr bool kRowScaled = ROW_FMT == 4;
+        const Nvfp4Scale ts_tensor = nvfp4_tensor_scale(kRowScaled ? 0.0f : a.row_amax[g]);
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
             float v[8];
@@ -439,8 +444,16 @@ __global__ void __launch_bounds__(kThreads, 2) quantize_kernel(QuantArgs a)
             b = fmaxf(b, __shfl_xor_sync(0xFFFFFFFFu, b, 1));
             float e;
             uint32_t S;
-            if constexpr (kRowTab) S = nvfp4_block_scale(ts, q_tab[0], b, e);
-            else S = nvfp4_block_scale_div(ts, b, e);
+            if constexpr (kRowScaled) {
+                // the row's own amax (padded row index; rows past the stored ones read 0)
+                const int64_t pr = prow0 + i;
+                const float A_r = pr < a.row_rows_store ? a.row_amax[pr] : 0.0f;
+                S = nvfp4_block_scale_div(nvfp4_tensor_scale(A_r), b, e);
+            } else if constexpr (kRowTab) {
+                S = nvfp4_block_scale(ts_tensor, q_tab[0], b, e);
+            } else {
+                S = nvfp4_block_scale_div(ts_tensor, b, e);
+            }
             const int64_t p = prow0 + i;
             const uint64_t L0 = (uint64_t)p * (uint64_t)a.K + (uint64_t)k0;
             const uint32_t codes = nvfp4_encode8<SR>(v, e, L0, 0, a);
@@ -506,9 +519,20 @@ __global__ void __launch_bounds__(kThreads, 2) quantize_kernel(QuantArgs a)
 
     // ---------------- columnwise direction (output row = column k, contraction = padded row p)
     if (!col_pass) {
-    } else if constexpr (COL_FMT == 1) {  // NVFP4: the thread's 16 rows form one block per column
+    } else if constexpr (COL_FMT == 1 || COL_FMT == 5) {  // NVFP4: the thread's 16 rows form one block per column
         const Nvfp4Scale ts = nvfp4_tensor_scale(a.col_amax[g]);
         if constexpr (RHT) flip_rows(t, a.rht_sign_mask);  // the rowwise pass is done with t
+        float tile_b = 0.0f;  // 2D: amax of the 16 x 16 tile (this lane's 16 x 8 and lane ^ 1's)
+        if constexpr (COL_FMT == 5) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                float v[8];
+                unpack8(t.w[i], v);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) tile_b = fmaxf(tile_b, fabsf(v[j]));
+            }
+            tile_b = fmaxf(tile_b, __shfl_xor_sync(0xFFFFFFFFu, tile_b, 1));
+        }
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             float u[16];
@@ -517,6 +541,7 @@ __global__ void __launch_bounds__(kThreads, 2) quantize_kernel(QuantArgs a)
             float b = 0.0f;
 #pragma unroll
             for (int i = 0; i < 16; ++i) b = fmaxf(b, fabsf(u[i]));
+            if constexpr (COL_FMT == 5) b = tile_b;
             float e;
             const uint32_t S = nvfp4_block_scale(ts, q_tab[1], b, e);
             const int64_t k = k0 + j;
@@ -573,9 +598,9 @@ __global__ void __launch_bounds__(kThreads, 2) quantize_kernel(QuantArgs a)
     // ---------------- write-out of staged outputs
     const int64_t p_tile0 = tile_row * kTileRows;
     if (!row_out) {
-    } else if constexpr (ROW_FMT == 1 || ROW_FMT == 2) {
+    } else if constexpr (ROW_FMT == 1 || ROW_FMT == 2 || ROW_FMT == 4) {
         // this CTA's scale columns: NVFP4 16 (4 tiles), MXFP8 8 (2 tiles), all in tile-row tile_row
-        constexpr int ntiles = ROW_FMT == 1 ? 4 : 2;
+        constexpr int ntiles = ROW_FMT == 2 ? 2 : 4;
         const int64_t ct0 = tile_col * ntiles;
         for (int i = threadIdx.x; i < ntiles * 32; i += kThreads) {
             const int tt = i >> 5;
@@ -586,13 +611,14 @@ __global__ void __launch_bounds__(kThreads, 2) quantize_kernel(QuantArgs a)
         }
     }
     if (!col_pass) {
-    } else if constexpr (COL_FMT == 1 || COL_FMT == 2) {
-        const int64_t row_bytes = COL_FMT == 1 ? a.col_cols_store / 2 : a.col_cols_store;
-        const int64_t byte0 = COL_FMT == 1 ? p_tile0 / 2 : p_tile0;
+    } else if constexpr (COL_FMT == 1 || COL_FMT == 2 || COL_FMT == 5) {
+        constexpr bool kNv = COL_FMT != 2;
+        const int64_t row_bytes = kNv ? a.col_cols_store / 2 : a.col_cols_store;
+        const int64_t byte0 = kNv ? p_tile0 / 2 : p_tile0;
         for (int i = threadIdx.x; i < kTileCols * 8; i += kThreads) {
             const int kk = i >> 3, ch = i & 7;  // 8 chunks per output row
             const int64_t k = tile_col * kTileCols + kk;
-            if (COL_FMT == 1) {
+            if (kNv) {
                 const int64_t off = byte0 + ch * 8;
                 if (k < a.K && off < row_bytes)
                     *reinterpret_cast<uint2*>(a.col_data + k * row_bytes + off) =
@@ -605,8 +631,8 @@ __global__ void __launch_bounds__(kThreads, 2) quantize_kernel(QuantArgs a)
             }
         }
         // scales: output rows k (two 128-row tile-rows), scale columns p/16 (NVFP4, 2 tiles) or p/32 (1 tile)
-        constexpr int nct = COL_FMT == 1 ? 2 : 1;
-        const int64_t ct0 = COL_FMT == 1 ? (p_tile0 / 16) / 4 : (p_tile0 / 32) / 4;
+        constexpr int nct = kNv ? 2 : 1;
+        const int64_t ct0 = kNv ? (p_tile0 / 16) / 4 : (p_tile0 / 32) / 4;
         for (int i = threadIdx.x; i < 2 * nct * 32; i += kThreads) {
             const int kt = i / (nct * 32), rem = i % (nct * 32), tt = rem >> 5, chunk = rem & 31;
             const int64_t ktile = tile_col * 2 + kt;  // 128-row tile of the output rows

@@ -13,12 +13,12 @@ def bits(t: torch.Tensor) -> np.ndarray:
 
 def qt_codes(q: nvq.QTensor) -> np.ndarray:
     """GPU codes as [rows, bytes per row]."""
-    per_row = q.cols // 2 if q.fmt == nvq.NVFP4 else q.cols
+    per_row = q.cols // 2 if q.fmt in (nvq.NVFP4, nvq.NVFP4_ROWSCALED) else q.cols
     return q.data[: q.rows * per_row].cpu().numpy().reshape(q.rows, per_row)
 
 
 def qt_scales(q: nvq.QTensor) -> np.ndarray:
-    blk = 16 if q.fmt == nvq.NVFP4 else 32
+    blk = 16 if q.fmt in (nvq.NVFP4, nvq.NVFP4_ROWSCALED) else 32
     n = oracle.swizzled_size(q.rows, q.cols // blk)
     return q.scale[:n].cpu().numpy()
 
