@@ -42,9 +42,9 @@ FP4_OVER_BF16 = 6.0
 # current kernels on this workload (profiles/gemm_pair_nvfp4_llama3_8b_fwd.md: the
 # forward GEMM launch; profiles/quantize_nvfp4_llama3_8b.md: the six amax + quantize
 # launches of one step).  Set to None whenever those kernels change.
-GEMM_TRAFFIC_BYTES = (107.147776 + 430.426624) * 1e6
-QUANT_TRAFFIC_BYTES = (134.263 + 2.949 + 134.287 + 39.597 + 117.468 + 0.084
-                       + 117.494 + 29.759 + 469.811 + 0.137 + 469.907 + 228.597) * 1e6
+GEMM_TRAFFIC_BYTES = (105.395456 + 426.097408) * 1e6
+QUANT_TRAFFIC_BYTES = (134.247936 + 2.951680 + 134.289408 + 39.681792 + 117.468416 + 0.214784
+                       + 117.492224 + 29.814528 + 469.817856 + 0.406784 + 470.241280 + 228.738560) * 1e6
 
 
 def _env_int(name, default):
