@@ -752,6 +752,134 @@ def run_qwen3_stack(args, nvq, inputs):
             "tokens_per_s": Tk / (ms * 1e-3)}
 
 
+def run_variants(args, nvq, inputs):
+    """The recipe variants beside the base paths they extend, at the Llama-3-8B
+    up-projection shapes (x[16384,4096], W[14336,4096]) and the MoE workload:
+
+      amax_chain   forward GEMM with and without its output amaxes (plain + Hadamard
+                   domain) in the epilogue; x's quantization with the amax given vs measured
+      dequant_src  x: NVFP4 rows with an MXFP8 / NVFP4 / identity columnwise direction built
+                   from the dequantized rowwise value (columnwise_source = rowwise_dequantized)
+      row_scaled   MoE x[65536,4096]: row-scaled NVFP4 rows + MXFP8 columns, and the grouped
+                   forward GEMM with a row-scaled A vs a per-group-scaled A
+      two_d        W: MXFP8 rows + NVFP4 columns with 16x16 tile scales vs 1x16 blocks
+      hybrid_linear  MXFP8 forward + NVFP4 backward step (W columns 2D) vs the NVFP4 step
+
+    Quantize rates are algorithmic bytes (each pass's bf16 read + the outputs written) per
+    second; GEMM / step rates are FLOPs per second.  Inputs above L2 are timed back to back
+    from a CUDA graph, those below it with L2 flushed before each call."""
+    import torch
+    sign = inputs.rht_sign_vector()
+    sr = (inputs.SR_SEED, 0)
+    Mq, Nq, Kq = inputs.LLAMA3_8B_UP["M"], inputs.LLAMA3_8B_UP["N"], inputs.LLAMA3_8B_UP["K"]
+    xh, wh, dyh = inputs.llama_up()
+    x, w, dy = xh.cuda(), wh.cuda(), dyh.cuda()
+    del xh, wh, dyh
+    al, cc = nvq.alloc_qtensor, nvq.colwise_cols
+    out = {}
+
+    def timed(fn, nbytes_in):
+        small = nbytes_in < 129e6
+        return _flushed_ms(fn, max(5, args.steps), args.warmup) if small else _graph_ms(fn, args.steps, args.warmup)
+
+    def gbs(b, ms):
+        return b / (ms * 1e-3) / 1e9
+
+    ex = Mq * Kq
+    # ---- f-1: the amax produced upstream
+    xr, xcol = al(nvq.NVFP4, Mq, Kq), al(nvq.NVFP4, Kq, cc(nvq.NVFP4, Mq))
+    wr = al(nvq.NVFP4, Nq, Kq)
+    nvq.nvfp4_quantize(x, 3, rht_sign=sign, out_row=xr, out_col=xcol)
+    nvq.nvfp4_quantize(w, nvq.DIR_ROW, out_row=wr)
+    y = torch.empty(Mq, Nq, dtype=torch.bfloat16, device="cuda")
+    a1, a2 = torch.empty(1, device="cuda"), torch.empty(1, device="cuda")
+    gflop = 2.0 * Mq * Nq * Kq
+    t_plain = timed(lambda: nvq.gemm_tn(xr, wr, out=y), 1e12)
+    t_amax = timed(lambda: nvq.gemm_tn(xr, wr, out=y, rht_sign=sign, amax_out=a1, amax_rht_out=a2), 1e12)
+    t_meas = timed(lambda: nvq.nvfp4_quantize(x, 3, rht_sign=sign, out_row=xr, out_col=xcol), ex * 2)
+    t_given = timed(lambda: nvq.nvfp4_quantize(x, 3, rht_sign=sign, out_row=xr, out_col=xcol, amax_given=True), ex * 2)
+    out["amax_chain"] = {
+        "gemm_fwd_ms": t_plain, "gemm_fwd_with_output_amaxes_ms": t_amax,
+        "gemm_tflops": gflop / (t_plain * 1e-3) / 1e12, "gemm_with_amax_tflops": gflop / (t_amax * 1e-3) / 1e12,
+        "x_quantize_measured_amax_ms": t_meas, "x_quantize_given_amax_ms": t_given,
+        "x_quantize_measured_gbs": gbs(ex * 5.125, t_meas), "x_quantize_given_gbs": gbs(ex * 3.125, t_given),
+        "bytes_per_element": {"measured": 5.125, "given": 3.125}}
+    # ---- f-2: rowwise-dequantized source
+    dq = nvq.COL_SOURCE_ROWWISE_DEQUANTIZED
+    cols = {nvq.MXFP8: al(nvq.MXFP8, Kq, cc(nvq.MXFP8, Mq)), nvq.NVFP4: xcol,
+            nvq.IDENTITY: al(nvq.IDENTITY, Kq, cc(nvq.IDENTITY, Mq))}
+    bpe = {nvq.MXFP8: 2 + 2 + 0.5625 + 1.03125, nvq.NVFP4: 2 + 2 + 2 + 0.5625 + 0.5625,
+           nvq.IDENTITY: 2 + 2 + 0.5625 + 2.0}
+    names = {nvq.MXFP8: "nvfp4_row_mxfp8_col", nvq.NVFP4: "nvfp4_row_nvfp4_col", nvq.IDENTITY: "nvfp4_row_identity_col"}
+    d = {}
+    for cf, q in cols.items():
+        t = timed(lambda q=q, cf=cf: nvq.hybrid_quantize(x, nvq.NVFP4, cf, out_row=xr, out_col=q, col_source=dq), ex * 2)
+        d[names[cf]] = {"ms": t, "GB/s": gbs(ex * bpe[cf], t), "bytes_per_element": bpe[cf]}
+    t = timed(lambda: nvq.hybrid_quantize(x, nvq.NVFP4, nvq.MXFP8, out_row=xr, out_col=cols[nvq.MXFP8]), ex * 2)
+    d["original_source_nvfp4_row_mxfp8_col"] = {"ms": t, "GB/s": gbs(ex * bpe[nvq.MXFP8], t)}
+    out["dequant_src"] = d
+    del cols
+    # ---- f-4: 2D columnwise scaling of W, and the hybrid-format linear step
+    ew = Nq * Kq
+    wrm, wc2 = al(nvq.MXFP8, Nq, Kq), al(nvq.NVFP4, Kq, cc(nvq.NVFP4, Nq))
+    b2d = 2 + 2 + 1.03125 + 0.5625
+    t2 = timed(lambda: nvq.hybrid_quantize(w, nvq.MXFP8, nvq.NVFP4, out_row=wrm, out_col=wc2, col_2d=True), ew * 2)
+    t1 = timed(lambda: nvq.hybrid_quantize(w, nvq.MXFP8, nvq.NVFP4, out_row=wrm, out_col=wc2), ew * 2)
+    out["two_d"] = {"w_mxfp8_row_nvfp4_2d_col": {"ms": t2, "GB/s": gbs(ew * b2d, t2)},
+                    "w_mxfp8_row_nvfp4_1d_col": {"ms": t1, "GB/s": gbs(ew * b2d, t1)}, "bytes_per_element": b2d}
+    del wrm, wc2
+    ybuf = torch.empty(Mq, Nq, dtype=torch.bfloat16, device="cuda")
+    dxb = torch.empty(Mq, Kq, dtype=torch.bfloat16, device="cuda")
+    dwb = torch.empty(Nq, Kq, dtype=torch.bfloat16, device="cuda")
+    hb = {}
+
+    def hstep():
+        _, hb["f"] = nvq.hybrid_linear_fwd(x, w, nvq.MXFP8, nvq.NVFP4, rht_sign=sign, w_col_2d=True, y=ybuf,
+                                           bufs=hb.get("f"))
+        hb["b"] = nvq.hybrid_linear_bwd_quantize(dy, nvq.NVFP4, rht_sign=sign, sr=sr, bufs=hb.get("b"))
+        nvq.linear_dgrad(hb["b"]["dy_row"], hb["f"]["w_col"], dx=dxb)
+        nvq.linear_wgrad(hb["b"]["dy_col"], hb["f"]["x_col"], dw=dwb)
+
+    hstep()
+    th = _graph_ms(hstep, args.steps, args.warmup)
+    out["hybrid_linear"] = {"mxfp8_fwd_nvfp4_bwd_step_ms": th, "TFLOP/s": 3 * gflop / (th * 1e-3) / 1e12,
+                            "note": "x, W MXFP8 rows + NVFP4 columns (x RHT, W 2D), dy NVFP4 SR + RHT; fwd MXFP8 GEMM, "
+                                    "dgrad / wgrad NVFP4"}
+    del hb, ybuf, dxb, dwb, y, x, w, dy, xr, xcol, wr
+    torch.cuda.empty_cache()
+    # ---- f-3: row-scaled NVFP4 on the MoE workload
+    sizes, xm, wm, _ = inputs.moe_grouped()
+    sizes = [int(v) for v in sizes]
+    G, Nn, Km = wm.shape
+    xm = xm.cuda()
+    w2 = wm.reshape(G * Nn, Km).cuda()
+    del wm
+    P = nvq.grouped_padded_rows(sizes)
+    T = sum(sizes)
+    xrs, xrp = al(nvq.NVFP4_ROWSCALED, P, Km), al(nvq.NVFP4, P, Km, n_amax=G)
+    xcm = al(nvq.MXFP8, Km, P)
+    wrg, _ = nvq.grouped_hybrid_quantize(w2, [Nn] * G, nvq.NVFP4, nvq.NONE)
+    ym = torch.empty(T, Nn, dtype=torch.bfloat16, device="cuda")
+    em = T * Km
+    brs = 2 + 2 + 0.5625 + 1.03125
+    trs = timed(lambda: nvq.grouped_hybrid_quantize(xm, sizes, nvq.NVFP4_ROWSCALED, nvq.MXFP8, out_row=xrs, out_col=xcm),
+                em * 2)
+    tpg = timed(lambda: nvq.grouped_hybrid_quantize(xm, sizes, nvq.NVFP4, nvq.MXFP8, out_row=xrp, out_col=xcm), em * 2)
+    mflop = 2.0 * T * Nn * Km
+    tgr = timed(lambda: nvq.grouped_gemm_rows(xrs, wrg, sizes, Nn, b_col_groups=False, out=ym), 1e12)
+    tgp = timed(lambda: nvq.grouped_gemm_rows(xrp, wrg, sizes, Nn, b_col_groups=False, out=ym), 1e12)
+    out["row_scaled"] = {"x_quantize_row_scaled_ms": trs, "x_quantize_row_scaled_GB/s": gbs(em * brs, trs),
+                         "x_quantize_per_group_ms": tpg, "x_quantize_per_group_GB/s": gbs(em * brs, tpg),
+                         "grouped_fwd_row_scaled_ms": tgr, "grouped_fwd_row_scaled_TFLOP/s": mflop / (tgr * 1e-3) / 1e12,
+                         "grouped_fwd_per_group_ms": tgp, "grouped_fwd_per_group_TFLOP/s": mflop / (tgp * 1e-3) / 1e12,
+                         "bytes_per_element": brs}
+    peaks, src = _peaks()
+    return {"metric": "recipe variants (amax chain, rowwise-dequantized source, row scaling, 2D scaling, hybrid linear)",
+            "value": out["hybrid_linear"]["TFLOP/s"], "unit": "TFLOP/s (hybrid-format linear step)",
+            "variants": out, "hbm_peak_gbs": peaks["hbm_gbs"], "peak_source": src, "dtype": "mixed",
+            "config": {"workload": "recipe_variants_llama3_8b_up_and_moe"}}
+
+
 def run_single_linear(args, nvq, inputs):
     """x, W bf16[256,512]: quantize both rowwise and y = x W^T (latency)."""
     x, w = inputs.single_linear()
@@ -784,7 +912,7 @@ def run_workload(args, rank, world, local_rank):
     __graft_entry__.build()
     torch.cuda.set_device(local_rank)
     fn = {"quant_sweep": run_quant_sweep, "moe_grouped": run_moe_grouped, "qwen3_stack": run_qwen3_stack,
-          "single_linear": run_single_linear}[args.workload]
+          "single_linear": run_single_linear, "variants": run_variants}[args.workload]
     clocks = ClockSampler(local_rank)
     clocks.start()
     r = fn(args, nvq, inputs)
@@ -813,7 +941,7 @@ def main():
     ap.add_argument("--no-amax-chain", action="store_true",
                     help="qwen3_stack: measure every amax with its own pass instead of taking it from the producing GEMM")
     ap.add_argument("--workload", default="llama_up",
-                    choices=["llama_up", "quant_sweep", "moe_grouped", "qwen3_stack", "single_linear"],
+                    choices=["llama_up", "quant_sweep", "moe_grouped", "qwen3_stack", "single_linear", "variants"],
                     help="llama_up (default: the headline line) or one of the other configurations")
     args = ap.parse_args()
     if args.oracle_child is not None:

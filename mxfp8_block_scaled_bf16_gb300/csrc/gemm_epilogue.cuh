@@ -69,6 +69,64 @@ __device__ __forceinline__ void epi_amax_add_bf16(EpiAmax& am, const uint32_t* w
     }
 }
 
+// Packed fp32 pairs (element 0 in the low word): one instruction adds or
+// subtracts both, each lane rounded to nearest as a scalar fp32 add would be.
+__device__ __forceinline__ uint64_t f32x2_add(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+__device__ __forceinline__ uint64_t f32x2_sub(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// Both amaxes of a 32-row x 64-column bf16 block staged in shared memory for a
+// TMA store (row r at r * 128 bytes, 16-byte chunks XOR-swizzled by r & 7), read
+// back by columns: lane l takes columns 2l and 2l + 1 (one 4-byte word per row;
+// the 32 lanes read a row's 128 bytes, one word per bank) and runs the
+// Hadamard butterfly of each 16-row block in registers on packed fp32 pairs.
+// Replaces the lane-shuffle form on this path (four shuffles per value made
+// the epilogue, not the tensor core, set the tile rate).
+__device__ __forceinline__ void epi_amax_add_staged(EpiAmax& am, const GemmArgs& args, const uint8_t* stage, int lane)
+{
+    if (!am.on_plain && !am.on_rht) return;
+    const int chunk = lane >> 2, within = (lane & 3) * 4;
+#pragma unroll
+    for (int blk = 0; blk < 2; ++blk) {
+        uint64_t v[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int r = 16 * blk + i;
+            uint32_t w = *reinterpret_cast<const uint32_t*>(stage + r * 128 + ((chunk ^ (r & 7)) << 4) + within);
+            am.plain = fmaxf(am.plain, fmaxf(fabsf(__uint_as_float(w << 16)), fabsf(__uint_as_float(w & 0xFFFF0000u))));
+            if (am.on_rht && ((args.rht_sign_mask >> i) & 1u)) w ^= 0x80008000u;  // s .* u (row i of the block)
+            v[i] = ((uint64_t)(w & 0xFFFF0000u) << 32) | (uint64_t)(w << 16);
+        }
+        if (am.on_rht) {
+#pragma unroll
+            for (int h = 1; h < 16; h <<= 1) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    if ((i & h) == 0) {
+                        const uint64_t a = v[i], b = v[i + h];
+                        v[i] = f32x2_add(a, b);
+                        v[i + h] = f32x2_sub(a, b);
+                    }
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                am.rht = fmaxf(am.rht, fmaxf(fabsf(__uint_as_float((uint32_t)v[i])),
+                                             fabsf(__uint_as_float((uint32_t)(v[i] >> 32)))));
+        }
+    }
+}
+
 __device__ __forceinline__ float epi_warp_max(float v)
 {
 #pragma unroll
@@ -233,7 +291,6 @@ __device__ __forceinline__ void epilogue_slice_tma(const GemmArgs& args, const C
         uint32_t packed[32];
         pack32_bf16(args, v[2 * b], alpha, col0 + 64 * b, &packed[0]);
         pack32_bf16(args, v[2 * b + 1], alpha, col0 + 64 * b + 32, &packed[16]);
-        epi_amax_add_bf16<32>(am, packed);
         if (lane == 0) bulk_wait_group_read0();  // the previous store has read the buffer
         __syncwarp();
 #pragma unroll
@@ -246,6 +303,9 @@ __device__ __forceinline__ void epilogue_slice_tma(const GemmArgs& args, const C
             tma_store_2d(c_map, stage, col0 + 64 * b, c_row0);
             bulk_commit_group();
         }
+        // the output amaxes from the staged block (read while the store reads it;
+        // the next half's writes wait for every lane at the __syncwarp above)
+        epi_amax_add_staged(am, args, stage, lane);
     }
 }
 
