@@ -69,22 +69,6 @@ __device__ __forceinline__ void epi_amax_add_bf16(EpiAmax& am, const uint32_t* w
     }
 }
 
-// Packed fp32 pairs (element 0 in the low word): one instruction adds or
-// subtracts both, each lane rounded to nearest as a scalar fp32 add would be.
-__device__ __forceinline__ uint64_t f32x2_add(uint64_t a, uint64_t b)
-{
-    uint64_t d;
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-
-__device__ __forceinline__ uint64_t f32x2_sub(uint64_t a, uint64_t b)
-{
-    uint64_t d;
-    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-
 // Both amaxes of a 32-row x 64-column bf16 block staged in shared memory for a
 // TMA store (row r at r * 128 bytes, 16-byte chunks XOR-swizzled by r & 7), read
 // back by columns: lane l takes columns 2l and 2l + 1 (one 4-byte word per row;
@@ -114,8 +98,8 @@ __device__ __forceinline__ void epi_amax_add_staged(EpiAmax& am, const GemmArgs&
                 for (int i = 0; i < 16; ++i) {
                     if ((i & h) == 0) {
                         const uint64_t a = v[i], b = v[i + h];
-                        v[i] = f32x2_add(a, b);
-                        v[i + h] = f32x2_sub(a, b);
+                        v[i] = f2_add_rn(a, b);
+                        v[i + h] = f2_sub_rn(a, b);
                     }
                 }
             }

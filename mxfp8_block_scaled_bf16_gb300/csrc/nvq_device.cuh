@@ -614,29 +614,116 @@ __device__ __forceinline__ uint32_t e2m1x8_rn(const float (&v)[8])
     return out;
 }
 
-// Stochastic rounding of v onto the E2M1 grid with 16 random bits r: the
-// magnitude between neighbours lo <= |v| < hi (spacing q) rounds up iff
-// r < ceil(2^16 (|v| - lo) / q); saturates at 6; keeps the sign.  Computed as
-// idx = ceil(|v|/q - r/2^16), magnitude idx * q, which is the same decision:
-// with |v|/q = n + f, ceil(n + f - r/2^16) = n + [f > r/2^16] and, r being an
-// integer, f > r/2^16 <=> r < ceil(2^16 f).  Every step is exact in fp32:
-// |v|/q is a power-of-two scaling, r/2^16 is built from the bit pattern
-// 1.r (no conversion instruction), |v|/q - r/2^16 needs at most 24
-// significant bits, and ceil() of a value in (-1, 4) is a round-up add of
-// 1.5 * 2^23.  q = max(2^(floor(log2 |v|) - 1), 1/2) comes from the exponent
-// bits.  |v| >= 6 is not clamped first: it lands on a grid multiple >= 6 (at
-// most 3 * 2^126, finite), which the saturating round-to-nearest encode maps
-// to 6 like the saturation rule.  r_mant holds r in mantissa bits 7..22
-// (r << 7).  Returns the grid value, to be encoded by round-to-nearest.
-__device__ __forceinline__ float e2m1_sr_value(float v, uint32_t r_mant)
+// ------------------------------------------------------------------ packed fp32 pairs
+// Two fp32 values in one 64-bit register pair (element 0 in the low word); the
+// f32x2 instructions apply one IEEE operation, with the stated rounding, to
+// each half -- the same result as two scalar operations in one issue slot.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi)
 {
-    const float q = fmaxf(__uint_as_float((__float_as_uint(v) & 0x7F800000u) - 0x00800000u), 0.5f);
-    const float inv_q = __uint_as_float(0x7F000000u - __float_as_uint(q));
-    const float rf = __fsub_rn(__uint_as_float(0x3F800000u | r_mant), 1.0f);
-    const float d = __fmaf_rn(fabsf(v), inv_q, -rf);
-    const float c = __fsub_rn(__fadd_ru(d, 12582912.0f), 12582912.0f);
-    return copysignf(__fmul_rn(c, q), v);
+    return ((uint64_t)__float_as_uint(hi) << 32) | (uint64_t)__float_as_uint(lo);
 }
+__device__ __forceinline__ float f2_lo(uint64_t v) { return __uint_as_float((uint32_t)v); }
+__device__ __forceinline__ float f2_hi(uint64_t v) { return __uint_as_float((uint32_t)(v >> 32)); }
+
+__device__ __forceinline__ uint64_t f2_add_rn(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_sub_rn(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_add_rp(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm("add.rp.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_mul_rn(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_fma_rn(uint64_t a, uint64_t b, uint64_t c)
+{
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_fma_rp(uint64_t a, uint64_t b, uint64_t c)
+{
+    uint64_t d;
+    asm("fma.rp.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ float fmin3(float a, float b, float c)
+{
+    float d;
+    asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c)
+{
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// ------------------------------------------------------------------ stochastic rounding to E2M1
+// Stochastic rounding of a pair of values onto the E2M1 grid with 16 random
+// bits r each, as E2M1 codes: a magnitude between neighbours lo <= |v| < hi
+// rounds up iff r < ceil(2^16 (|v| - lo) / (hi - lo)); 6 and above saturate;
+// the sign is kept.  Computed in the index domain, where the grid
+// {0, .5, 1, 1.5, 2, 3, 4, 6} becomes the integers 0..7:
+// idx(x) = min(2x, x + 2, x/2 + 4) is the concave piecewise-linear map that
+// sends each grid interval linearly onto [k, k + 1], so frac is the
+// fractional part of idx and the code is ceil(idx - r/2^16).
+//  - x = min(|v|, 6): values at or above 6 give idx = 7, code 7.
+//  - The three lines are formed with 128 added, one round-up fma / add each:
+//    on [128, 256) the fp32 ulp is 2^-16, the grid of r, and rounding frac up
+//    onto that grid moves no ceiling, so the minimum of the rounded lines
+//    gives the same decision (the sign of idx - r/2^16 when |v| < 0.5).
+//  - d = (128 + idx) - (128 + r/2^16) is exact; fl_ru(d + 1.5 * 2^23, + 8 for
+//    a negative v) holds ceil(d) (+ 8) in its low mantissa bits: the code
+//    nibble, sign included.
+// A CPU sweep checks this against the rounding rule on every finite bf16
+// value and 2.9e8 (value, r) pairs (tests/test_sr_formulation.py).
+//   v2:    the two values (v_lo, v_hi);
+//   negr2: the two values -(128 + r / 2^16), from sr_neg_r;
+//   z_lo, z_hi: bit patterns whose low nibbles are the two codes.
+__device__ __forceinline__ void e2m1_sr_pair(uint64_t v2, uint64_t negr2, uint32_t& z_lo, uint32_t& z_hi)
+{
+    const uint64_t kTwo = 0x4000000040000000ull, kHalf = 0x3F0000003F000000ull;
+    const uint64_t k128 = 0x4300000043000000ull, k130 = 0x4302000043020000ull, k132 = 0x4304000043040000ull;
+    const uint64_t kNegOne = 0xBF800000BF800000ull, kMagic4 = 0x4B4000044B400004ull;  // 1.5 * 2^23 + 4
+    const float vl = f2_lo(v2), vh = f2_hi(v2);
+    const uint64_t x = f2_pack(fminf(fabsf(vl), 6.0f), fminf(fabsf(vh), 6.0f));
+    const uint64_t a = f2_fma_rp(x, kTwo, k128);
+    const uint64_t b = f2_add_rp(x, k130);
+    const uint64_t c = f2_fma_rp(x, kHalf, k132);
+    const uint64_t m = f2_pack(fmin3(f2_lo(a), f2_lo(b), f2_lo(c)), fmin3(f2_hi(a), f2_hi(b), f2_hi(c)));
+    const uint64_t d = f2_add_rn(m, negr2);
+    const uint64_t sgn4 = f2_pack(copysignf(4.0f, vl), copysignf(4.0f, vh));
+    const uint64_t z = f2_add_rp(d, f2_fma_rn(sgn4, kNegOne, kMagic4));  // + 1.5 * 2^23 (+ 8 for a negative v)
+    z_lo = (uint32_t)z;
+    z_hi = (uint32_t)(z >> 32);
+}
+
+// -(128 + r / 2^16) for the 16-bit field `half` (0 low, 1 high) of a Philox word.
+__device__ __forceinline__ float sr_neg_r(uint32_t w, int half)
+{
+    return __uint_as_float(__byte_perm(w, 0xC3000000u, half ? 0x7432u : 0x7410u));
+}
+
+// Horner packing of 8 code nibbles from e2m1_sr_pair's bit patterns (each
+// 0x4B4000cc): sum_j bits_j * 16^j mod 2^32 carries the constant
+// 0x4B400000 * 0x11111111 on top of the packed codes.
+constexpr uint32_t kSrPackBias = 0x4B400000u * 0x11111111u;
 
 // ------------------------------------------------------------------ Philox4x32-10
 struct Philox4 {
@@ -662,12 +749,11 @@ __device__ __forceinline__ Philox4 philox4x32_10_rk(uint32_t c0, uint32_t c1, ui
     return {c0, c1, c2, c3};
 }
 
-// 16-bit random field f (0..7) of a Philox block (field 2i is the low half
-// of word i, 2i+1 the high half), placed in mantissa bits 7..22.
-__device__ __forceinline__ uint32_t philox_field_mant(const Philox4& p, int f)
+// Word i (0..3) of a Philox block: it holds the 16-bit random fields 2i (low
+// half) and 2i + 1 (high half).
+__device__ __forceinline__ uint32_t philox_word(const Philox4& p, int i)
 {
-    const uint32_t w = (f >> 1) == 0 ? p.x : (f >> 1) == 1 ? p.y : (f >> 1) == 2 ? p.z : p.w;
-    return ((f & 1) ? (w >> 9) : (w << 7)) & 0x007FFF80u;
+    return i == 0 ? p.x : i == 1 ? p.y : i == 2 ? p.z : p.w;
 }
 
 }  // namespace nvq

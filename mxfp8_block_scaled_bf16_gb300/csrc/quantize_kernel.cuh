@@ -141,6 +141,40 @@ __device__ __forceinline__ void hadamard16(float (&u)[16])
     for (int i = 0; i < 16; ++i) u[i] = __fmul_rn(u[i], 0.25f);
 }
 
+// The same transform on two columns at once (packed pairs): u2[i] holds row i
+// of both columns; butterflies with spans 1, 2, 4, 8, then the exact 1/4 when
+// quarter.
+template <bool kQuarter>
+__device__ __forceinline__ void hadamard16x2(uint64_t (&u2)[16])
+{
+#pragma unroll
+    for (int h = 1; h < 16; h <<= 1) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            if ((i & h) == 0) {
+                const uint64_t a = u2[i], b = u2[i + h];
+                u2[i] = f2_add_rn(a, b);
+                u2[i + h] = f2_sub_rn(a, b);
+            }
+        }
+    }
+    if constexpr (kQuarter) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) u2[i] = f2_mul_rn(u2[i], 0x3E8000003E800000ull);  // * 0.25, exact
+    }
+}
+
+// Columns 2m and 2m + 1 of the thread's tile (the two halves of word m) as 16
+// packed pairs, row 0 first.
+__device__ __forceinline__ void column_pair16(const ThreadTile& t, int m, uint64_t (&u2)[16])
+{
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const uint32_t w = m == 0 ? t.w[i].x : m == 1 ? t.w[i].y : m == 2 ? t.w[i].z : t.w[i].w;
+        u2[i] = ((uint64_t)(w & 0xFFFF0000u) << 32) | (uint64_t)(w << 16);
+    }
+}
+
 __device__ __forceinline__ void atomic_max_nonneg(float* addr, float v)
 {
     atomicMax(reinterpret_cast<unsigned int*>(addr), __float_as_uint(v));
@@ -286,17 +320,69 @@ template <bool SR>
 __device__ __forceinline__ uint32_t nvfp4_encode8(const float (&v)[8], float e, uint64_t L0, int dir,
                                                   const QuantArgs& a)
 {
-    float s[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) s[j] = __fmul_rn(v[j], e);
     if constexpr (SR) {
+        const uint64_t e2 = f2_pack(e, e);
+        uint64_t s2[4];  // v * e, elements (2h, 2h + 1) in pair h
+#pragma unroll
+        for (int h = 0; h < 4; ++h) s2[h] = f2_mul_rn(f2_pack(v[2 * h], v[2 * h + 1]), e2);
         const uint64_t blk = L0 >> 3;
         const Philox4 p = philox4x32_10_rk((uint32_t)blk, (uint32_t)(blk >> 32), (uint32_t)dir, a.sr_offset,
                                            a.sr_round_key);
+        uint32_t packed = 0;  // Horner over the elements, element 0 last (lowest nibble)
 #pragma unroll
-        for (int j = 0; j < 8; ++j) s[j] = e2m1_sr_value(s[j], philox_field_mant(p, j));
+        for (int h = 3; h >= 0; --h) {
+            const uint32_t w = philox_word(p, h);  // fields 2h (low half) and 2h + 1 (high half)
+            uint32_t zl, zh;
+            e2m1_sr_pair(s2[h], f2_pack(sr_neg_r(w, 0), sr_neg_r(w, 1)), zl, zh);
+            packed = packed * 16u + zh;
+            packed = packed * 16u + zl;
+        }
+        return packed - kSrPackBias;
+    } else {
+        float s[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) s[j] = __fmul_rn(v[j], e);
+        return e2m1x8_rn(s);
     }
-    return e2m1x8_rn(s);
+}
+
+// Two columns at once: v2[i] = (column A, column B) at row i of an 8-row
+// group, e2 = (e_A, e_B), LA0 / LB0 the linear indices of row 0 of each
+// column's group.  Codes of column A and column B, element 0 in the low nibble.
+template <bool SR>
+__device__ __forceinline__ void nvfp4_encode8x2(const uint64_t* v2, uint64_t e2, uint64_t LA0, uint64_t LB0, int dir,
+                                                const QuantArgs& a, uint32_t& codes_a, uint32_t& codes_b)
+{
+    uint64_t s2[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) s2[i] = f2_mul_rn(v2[i], e2);
+    if constexpr (SR) {
+        const uint64_t ba = LA0 >> 3, bb = LB0 >> 3;
+        const Philox4 pa = philox4x32_10_rk((uint32_t)ba, (uint32_t)(ba >> 32), (uint32_t)dir, a.sr_offset,
+                                            a.sr_round_key);
+        const Philox4 pb = philox4x32_10_rk((uint32_t)bb, (uint32_t)(bb >> 32), (uint32_t)dir, a.sr_offset,
+                                            a.sr_round_key);
+        uint32_t qa = 0, qb = 0;
+#pragma unroll
+        for (int i = 7; i >= 0; --i) {
+            const uint64_t nr = f2_pack(sr_neg_r(philox_word(pa, i >> 1), i & 1), sr_neg_r(philox_word(pb, i >> 1), i & 1));
+            uint32_t za, zb;
+            e2m1_sr_pair(s2[i], nr, za, zb);
+            qa = qa * 16u + za;
+            qb = qb * 16u + zb;
+        }
+        codes_a = qa - kSrPackBias;
+        codes_b = qb - kSrPackBias;
+    } else {
+        float sa[8], sb[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            sa[i] = f2_lo(s2[i]);
+            sb[i] = f2_hi(s2[i]);
+        }
+        codes_a = e2m1x8_rn(sa);
+        codes_b = e2m1x8_rn(sb);
+    }
 }
 
 // ------------------------------------------------------------------ MXFP8 block encode
@@ -533,29 +619,61 @@ __global__ void __launch_bounds__(kThreads, 2) quantize_kernel(QuantArgs a)
             }
             tile_b = fmaxf(tile_b, __shfl_xor_sync(0xFFFFFFFFu, tile_b, 1));
         }
+        if constexpr (RHT || SR) {
+        // columns 2m and 2m + 1 together, as packed pairs
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
+        for (int m = 0; m < 4; ++m) {
+            uint64_t u2[16];
+            column_pair16(t, m, u2);
+            if constexpr (RHT) hadamard16x2<true>(u2);
+            float b0 = 0.0f, b1 = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 16; i += 2) {
+                b0 = fmax3(b0, fabsf(f2_lo(u2[i])), fabsf(f2_lo(u2[i + 1])));
+                b1 = fmax3(b1, fabsf(f2_hi(u2[i])), fabsf(f2_hi(u2[i + 1])));
+            }
+            if constexpr (COL_FMT == 5) b0 = b1 = tile_b;
+            float e0, e1;
+            const uint32_t S0 = nvfp4_block_scale(ts, q_tab[1], b0, e0);
+            const uint32_t S1 = nvfp4_block_scale(ts, q_tab[1], b1, e1);
+            const uint64_t L0 = (uint64_t)(k0 + 2 * m) * (uint64_t)a.col_cols_store + (uint64_t)prow0;
+            const uint64_t L1 = L0 + (uint64_t)a.col_cols_store;
+            const uint64_t e2 = f2_pack(e0, e1);
+            uint32_t ca0, cb0, ca1, cb1;
+            nvfp4_encode8x2<SR>(&u2[0], e2, L0, L1, 1, a, ca0, cb0);
+            nvfp4_encode8x2<SR>(&u2[8], e2, L0 + 8, L1 + 8, 1, a, ca1, cb1);
+            const int kk = c_loc + 2 * m;  // output rows within the CTA (0..255): kk, kk + 1
+            const int c = r_loc / 16;      // scale column within the CTA (0..7)
+            *reinterpret_cast<uint2*>(&sm.col_codes[col_chunk_nv(kk, c)]) = make_uint2(ca0, ca1);
+            *reinterpret_cast<uint2*>(&sm.col_codes[col_chunk_nv(kk + 1, c)]) = make_uint2(cb0, cb1);
+            sm.col_scales[kk >> 7][(c >> 2) * 512 + (kk & 31) * 16 + ((kk >> 5) & 3) * 4 + (c & 3)] =
+                (uint8_t)(kvalid ? S0 : 0);
+            sm.col_scales[(kk + 1) >> 7][(c >> 2) * 512 + ((kk + 1) & 31) * 16 + (((kk + 1) >> 5) & 3) * 4 + (c & 3)] =
+                (uint8_t)(kvalid ? S1 : 0);
+        }
+        } else {
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) {
             float u[16];
-            column16(t, j, u);
-            if constexpr (RHT) hadamard16(u);
+            column16(t, jj, u);
             float b = 0.0f;
 #pragma unroll
             for (int i = 0; i < 16; ++i) b = fmaxf(b, fabsf(u[i]));
             if constexpr (COL_FMT == 5) b = tile_b;
             float e;
             const uint32_t S = nvfp4_block_scale(ts, q_tab[1], b, e);
-            const int64_t k = k0 + j;
-            const uint64_t Lbase = (uint64_t)k * (uint64_t)a.col_cols_store + (uint64_t)prow0;
+            const uint64_t Lbase = (uint64_t)(k0 + jj) * (uint64_t)a.col_cols_store + (uint64_t)prow0;
             float h0[8], h1[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) { h0[i] = u[i]; h1[i] = u[i + 8]; }
             const uint32_t c0 = nvfp4_encode8<SR>(h0, e, Lbase, 1, a);
             const uint32_t c1 = nvfp4_encode8<SR>(h1, e, Lbase + 8, 1, a);
-            *reinterpret_cast<uint2*>(&sm.col_codes[col_chunk_nv(c_loc + j, r_loc / 16)]) = make_uint2(c0, c1);
-            const int kk = c_loc + j;      // output row within CTA (0..255)
-            const int c = r_loc / 16;      // scale column within CTA (0..7)
+            *reinterpret_cast<uint2*>(&sm.col_codes[col_chunk_nv(c_loc + jj, r_loc / 16)]) = make_uint2(c0, c1);
+            const int kk = c_loc + jj;
+            const int c = r_loc / 16;
             sm.col_scales[kk >> 7][(c >> 2) * 512 + (kk & 31) * 16 + ((kk >> 5) & 3) * 4 + (c & 3)] =
                 (uint8_t)(kvalid ? S : 0);
+        }
         }
     } else if constexpr (COL_FMT == 2) {  // MXFP8: 32-blocks = this thread's 16 rows + lane^16's
 #pragma unroll
