@@ -42,9 +42,9 @@ FP4_OVER_BF16 = 6.0
 # current kernels on this workload (profiles/gemm_pair_nvfp4_llama3_8b_fwd.md: the
 # forward GEMM launch; profiles/quantize_nvfp4_llama3_8b.md: the six amax + quantize
 # launches of one step).  Set to None whenever those kernels change.
-GEMM_TRAFFIC_BYTES = (105.395456 + 426.097408) * 1e6
-QUANT_TRAFFIC_BYTES = (134.247936 + 2.951680 + 134.289408 + 39.681792 + 117.468416 + 0.214784
-                       + 117.492224 + 29.814528 + 469.817856 + 0.406784 + 470.241280 + 228.738560) * 1e6
+GEMM_TRAFFIC_BYTES = float(104373504 + 426027008)
+QUANT_TRAFFIC_BYTES = float(134246144 + 2973696 + 134285568 + 39769600 + 117470208 + 65280
+                            + 117523968 + 29878016 + 469813760 + 75520 + 469958144 + 229856512)
 
 
 def _env_int(name, default):

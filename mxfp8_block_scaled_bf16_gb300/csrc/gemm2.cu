@@ -361,23 +361,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         break;
                     }
                     tc_fence_after();
-                    const int left = tl.k_len - kb * C::kStageK;
-                    const int atoms = (min(C::kStageK, left) + C::kElemPerAtom - 1) / C::kElemPerAtom;
                     const uint32_t sfa_col = tmem_base + C::kSfCol0 + (uint32_t)s * C::kSfColsPerStage;
                     const uint32_t sfb_col = sfa_col + C::kSfaCols;
                     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
                     const uint8_t* sfa = smem + C::kSfa + s * C::kSfaBytes + lane * 16;
                     const uint8_t* sfb = smem + C::kSfb + s * C::kSfbBytes + lane * 16;
-#pragma unroll
-                    for (int j = 0; j < C::kAtomsK; ++j) {
-                        if (j < atoms) {
-                            tmem_st_32x32b_x1(sfa_col + lane_base + 4 * j + q, *reinterpret_cast<const uint32_t*>(sfa + 512 * j + 4 * q));
-#pragma unroll
-                            for (int h = 0; h < C::kSfbHalves; ++h)
-                                tmem_st_32x32b_x4(sfb_col + lane_base + 4 * (C::kSfbHalves * j + h),
-                                                  *reinterpret_cast<const uint4*>(sfb + 512 * (h * C::kAtomsK + j)));
-                        }
-                    }
+                    stage_block_scales<C::kAtomsK, C::kSfbHalves>(sfa_col, sfb_col, lane_base, q, sfa, sfb);
                     tmem_st_wait();
                     tc_fence_before();
                     __syncwarp();

@@ -432,6 +432,84 @@ __device__ __forceinline__ void tmem_st_32x32b_x4(uint32_t taddr, const uint4& v
                  : "memory");
 }
 
+// 32 lanes x N consecutive columns (N = 8, 16 or 32).
+template <int N>
+__device__ __forceinline__ void tmem_st_32x32b_xn(uint32_t taddr, const uint32_t (&r)[N])
+{
+    static_assert(N == 8 || N == 16 || N == 32, "store width");
+    if constexpr (N == 8) {
+        asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+                     "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                     : "memory");
+    } else if constexpr (N == 16) {
+        asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+                     "%12, %13, %14, %15, %16};" ::"r"(taddr),
+                     "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+                     "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+                     : "memory");
+    } else {
+        asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+                     "%12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, "
+                     "%31, %32};" ::"r"(taddr),
+                     "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+                     "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
+                     "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+                     "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+                     : "memory");
+    }
+}
+
+// One pipeline stage's block scales, shared memory -> TMEM, by the warp of
+// lane quadrant q (TMEM lanes 32q..32q+31; `lane_base` = their address bits).
+// The stage holds kAtomsK 128x4 scale tiles of A at `sfa` and kAtomsK x
+// kBHalves tiles of B at `sfb` (512 bytes each, this lane's 16-byte row
+// already added), laid out as the block-scaled MMA reads them:
+//   A: the word of atom j for the row of this lane goes to column
+//      sfa_col + 4j + q (the MMA reads column 4j + q in quadrant q);
+//   B: the whole 16-byte tile row of atom j, half h, goes to columns
+//      sfb_col + 4 (kBHalves j + h) .. + 3 in every quadrant.
+// Each operand leaves in one wide store: the A word is written to all four
+// columns of its atom (the three the MMA does not read in this quadrant get
+// copies), because one wide store per operand ran faster than one narrow
+// store per atom (forward GEMM 354 -> 334 us, dgrad 324 -> 295 us).  Atoms
+// past a ragged stage end are written too (stale shared memory, in bounds);
+// their MMAs are predicated off.
+template <int kAtomsK, int kBHalves>
+__device__ __forceinline__ void stage_block_scales(uint32_t sfa_col, uint32_t sfb_col, uint32_t lane_base, int q,
+                                                   const uint8_t* sfa, const uint8_t* sfb)
+{
+    if constexpr (kAtomsK == 1) {
+        const uint32_t w = *reinterpret_cast<const uint32_t*>(sfa + 4 * q);
+        tmem_st_32x32b_x4(sfa_col + lane_base, make_uint4(w, w, w, w));
+    } else {
+        uint32_t ra[4 * kAtomsK];
+#pragma unroll
+        for (int j = 0; j < kAtomsK; ++j) {
+            const uint32_t w = *reinterpret_cast<const uint32_t*>(sfa + 512 * j + 4 * q);
+            ra[4 * j] = ra[4 * j + 1] = ra[4 * j + 2] = ra[4 * j + 3] = w;
+        }
+        tmem_st_32x32b_xn<4 * kAtomsK>(sfa_col + lane_base, ra);
+    }
+    constexpr int kNb = 4 * kAtomsK * kBHalves;
+    if constexpr (kNb == 4) {
+        tmem_st_32x32b_x4(sfb_col + lane_base, *reinterpret_cast<const uint4*>(sfb));
+    } else {
+        uint32_t rb[kNb];
+#pragma unroll
+        for (int j = 0; j < kAtomsK; ++j)
+#pragma unroll
+            for (int h = 0; h < kBHalves; ++h) {
+                const uint4 u = *reinterpret_cast<const uint4*>(sfb + 512 * (h * kAtomsK + j));
+                const int c = 4 * (kBHalves * j + h);
+                rb[c] = u.x;
+                rb[c + 1] = u.y;
+                rb[c + 2] = u.z;
+                rb[c + 3] = u.w;
+            }
+        tmem_st_32x32b_xn<kNb>(sfb_col + lane_base, rb);
+    }
+}
+
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // ------------------------------------------------------------------ CTA pairs (clusters of 2)
