@@ -345,15 +345,20 @@ def run_ours(args, rank, world, local_rank):
     else:
         cpu_v, cpu_desc, cpu_threads, _ = oracle_sample(x_h, w_h, dy_h, sign)
         st_v, st_desc = oracle_single_thread()
+    # which GEMM kernel ran: the CTA pair unless the library fell back to the single-CTA kernel
+    pair = nvq.gemm_pair_available()
+    gemm_label = ("gemm_pair_kernel<NVFP4> (CTA pair; fwd, dgrad, wgrad)" if pair
+                  else "gemm_kernel<NVFP4> (single CTA; fwd, dgrad, wgrad)")
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "nvfp4", "data": "synthetic", "config": CONFIG,
         "gpu_launches": 9 * args.steps,
         "launch_mode": "eager" if args.eager else "cuda_graph",
-        "roofline": {"bound": "tensor", "kernel": "gemm_pair_kernel<NVFP4> (CTA pair; fwd, dgrad, wgrad)",
+        "roofline": {"bound": "tensor", "kernel": gemm_label,
                      "achieved": achieved, "peak": peak_fp4, "unit": "TFLOP/s", "frac": achieved / peak_fp4,
-                     "traffic": GEMM_TRAFFIC_BYTES, "traffic_note": "bytes per launch, ncu capture of the forward GEMM",
+                     "traffic": GEMM_TRAFFIC_BYTES if pair else None,
+                     "traffic_note": "bytes per launch, ncu capture of the forward GEMM (CTA-pair kernel)",
                      "peak_note": f"{src} bf16 burst x {FP4_OVER_BF16} (fp4/bf16 nominal dense ratio); the GEMMs "
                                   "are timed in a short eager pass, so the burst figure applies",
                      "frac_of_sustained": achieved / (peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
