@@ -361,7 +361,19 @@ NVQ_API int64_t nvq_grouped_padded_rows(const int64_t* group_rows, int G);
 
 /* Grouped hybrid quantization of bf16 x[sum m_g][K] (row-major, ld):
  * row -> [P_G][K] in row_fmt, col -> [K][P_G] in col_fmt, per-group amax.
- * RHT and SR are not supported here (NVQ_ERR_UNSUPPORTED if non-NULL). */
+ * rht_col and sr act as in nvq_hybrid_quantize (RHT on an NVFP4 columnwise
+ * direction, SR on NVFP4 directions; each may be NULL), for a grouped NVFP4
+ * backward ([TE] Description: "MXFP8 fwd and NVFP4 bwd (or vice versa)";
+ * [TT] "What changed": SR on the gradient, RHT on the wgrad operands):
+ *  - the 16-row Hadamard blocks of the columnwise direction never straddle
+ *    two groups (each group starts at a multiple of 128 padded rows), and the
+ *    transformed amax is taken per group;
+ *  - each group's columnwise operand quantizes its rows padded with zero rows
+ *    to a multiple of 128, every 16-row block included: with RHT a block of
+ *    pad rows transforms to signed zeros, whose codes keep the sign (0x8);
+ *  - an element's stochastic-rounding index is its position in the padded
+ *    output: P * K + k for rowwise element (padded row P, column k), and
+ *    k * P_G + P for columnwise element (k, P). */
 NVQ_API nvq_status nvq_grouped_hybrid_quantize(const void* x, int64_t K, int64_t ld,
                                        const int64_t* group_rows, int G, nvq_format row_fmt,
                                        nvq_format col_fmt, nvq_qtensor* row, nvq_qtensor* col,

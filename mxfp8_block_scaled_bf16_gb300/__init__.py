@@ -414,8 +414,11 @@ def grouped_padded_rows(group_rows: Sequence[int]) -> int:
 
 
 def grouped_hybrid_quantize(x: torch.Tensor, group_rows: Sequence[int], row_fmt: int, col_fmt: int,
-                            stream=None, out_row: Optional[QTensor] = None, out_col: Optional[QTensor] = None):
-    """Per-group hybrid quantization; storage padded to 128 rows per group."""
+                            stream=None, out_row: Optional[QTensor] = None, out_col: Optional[QTensor] = None,
+                            rht_sign=None, sr=None):
+    """Per-group hybrid quantization; storage padded to 128 rows per group.
+    rht_sign / sr: RHT on an NVFP4 columnwise direction, SR on NVFP4
+    directions (stochastic-rounding index = position in the padded output)."""
     M, K, ld = _bf16_2d(x)
     arr, G = _groups(group_rows)
     P = load().nvq_grouped_padded_rows(arr, G)
@@ -425,7 +428,7 @@ def grouped_hybrid_quantize(x: torch.Tensor, group_rows: Sequence[int], row_fmt:
     rc, cc = (row.c() if row else None), (col.c() if col else None)
     _check(load().nvq_grouped_hybrid_quantize(_ptr(x), K, ld, arr, G, row_fmt, col_fmt,
                                               ctypes.byref(rc) if rc else None, ctypes.byref(cc) if cc else None,
-                                              None, None, _stream(stream)), "nvq_grouped_hybrid_quantize")
+                                              _rht(rht_sign), _sr(sr), _stream(stream)), "nvq_grouped_hybrid_quantize")
     return row, col
 
 

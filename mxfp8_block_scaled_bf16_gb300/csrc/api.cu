@@ -722,8 +722,7 @@ nvq_status nvq_grouped_hybrid_quantize(const void* x, int64_t K, int64_t ld, con
                                        const nvq_rht* rht_col, const nvq_sr* sr, nvq_stream stream)
 {
     if (!group_rows) return NVQ_ERR_NULL;
-    if (rht_col || sr) return NVQ_ERR_UNSUPPORTED;
-    return quantize_impl(x, 0, K, ld, group_rows, G, row_fmt, col_fmt, nullptr, nullptr, row, col,
+    return quantize_impl(x, 0, K, ld, group_rows, G, row_fmt, col_fmt, rht_col, sr, row, col,
                          reinterpret_cast<cudaStream_t>(stream));
 }
 

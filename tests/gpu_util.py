@@ -74,10 +74,10 @@ def bf16_from_bits(b: np.ndarray) -> torch.Tensor:
     return torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(torch.bfloat16)
 
 
-def assert_gemm_close(got: torch.Tensor, ref64: np.ndarray, what: str, tol: float = 1e-3):
+def assert_gemm_close(got: torch.Tensor, ref64: np.ndarray, what: str, tol: float = 1e-3, ulp_frac: float = 0.999):
     """fp32 output: relative Frobenius error <= tol against the fp64 oracle.
     bf16 output: relative Frobenius error <= tol against the oracle rounded
-    once to bf16, and >= 99.9% of elements within one bf16 ulp of it."""
+    once to bf16, and >= ulp_frac of elements within one bf16 ulp of it."""
     g = got.detach().float().cpu().numpy().astype(np.float64)
     if got.dtype == torch.float32:
         ref = ref64
@@ -94,7 +94,7 @@ def assert_gemm_close(got: torch.Tensor, ref64: np.ndarray, what: str, tol: floa
             return np.where(v & 0x8000, -(v & 0x7FFF), v & 0x7FFF)
         ulps = np.abs(ordered(gb) - ordered(rb))
         frac = np.mean(ulps <= 1)
-        assert frac >= 0.999, f"{what}: only {frac:.5f} of elements within 1 bf16 ulp"
+        assert frac >= ulp_frac, f"{what}: only {frac:.5f} of elements within 1 bf16 ulp"
     return rel
 
 

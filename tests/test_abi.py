@@ -108,9 +108,11 @@ def test_host_validation_before_any_launch(lib):
     assert lib.nvq_gemm_tn(QTP(_qt(1, 128, 256)), QTP(_qt(1, 128, 256)), None, None, 128, 0, None) in (1, 6)
     # linear entry points: dims must be multiples of 128
     assert lib.nvq_nvfp4_linear_fwd(16, 16, None, 100, 128, 128, None, 16, QTP(r), QTP(r), None, None, None) == 2
-    # grouped: SR / RHT rejected, too many groups rejected
+    # grouped: SR / RHT validated like the ungrouped call (a sign entry other
+    # than +-1 is a shape error), too many groups rejected
     rows = (ctypes.c_int64 * 2)(3, 5)
-    sr = nvq._SR(1, 0)
-    assert lib.nvq_grouped_hybrid_quantize(16, 256, 256, rows, 2, 1, 2, QTP(r), QTP(c), None, QTP(sr), None) == 5
+    bad_sign = nvq._RHT((ctypes.c_int8 * 16)(*([1] * 15 + [0])))
+    assert lib.nvq_grouped_hybrid_quantize(16, 256, 256, rows, 2, 1, 1, QTP(_qt(1, 256, 256)),
+                                           QTP(_qt(1, 256, 256)), ctypes.byref(bad_sign), None, None) == 2
     many = (ctypes.c_int64 * 300)(*([1] * 300))
     assert lib.nvq_grouped_hybrid_quantize(16, 256, 256, many, 300, 1, 2, QTP(r), QTP(c), None, None, None) == 2

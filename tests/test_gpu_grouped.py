@@ -3,7 +3,11 @@
 "Hybrid quantization" (GroupedLinear, _hybrid_split_quantize, grouped GEMM):
 forward with NVFP4 rowwise input/weight, dgrad and wgrad with MXFP8 operands
 quantized columnwise from the original bf16, MXFP8 grad_output.  Empty groups
-must work (a zero-length contraction gives a zero weight gradient)."""
+must work (a zero-length contraction gives a zero weight gradient).  The
+grouped NVFP4 backward ("MXFP8 fwd and NVFP4 bwd (or vice versa)", with the
+torchtitan recipe's SR on the gradient and RHT on the wgrad operands) is
+checked with the stochastic-rounding index of each element at its position
+in the padded grouped output."""
 import numpy as np
 import pytest
 import torch
@@ -12,7 +16,7 @@ import oracle
 import mxfp8_block_scaled_bf16_gb300 as nvq
 from mxfp8_block_scaled_bf16_gb300 import inputs
 
-from gpu_util import assert_gemm_close, bits
+from gpu_util import assert_codes_equal, assert_gemm_close, assert_scales_equal, bits, qt_codes
 
 pytestmark = pytest.mark.gpu
 
@@ -111,3 +115,103 @@ def test_all_groups_empty():
     dw = nvq.grouped_gemm_wgrad(dyc, xc, sizes)
     torch.cuda.synchronize()
     assert dw.shape == (3, 128, 256) and torch.count_nonzero(dw).item() == 0
+
+
+def _pad_starts(sizes):
+    starts, p = [], 0
+    for m in sizes:
+        starts.append(p)
+        p += -(-m // 128) * 128
+    return starts, p
+
+
+def _grouped_nvfp4_oracle(xb, sizes, rht=None, sr=None):
+    """Oracle NVFP4 rows and columns of a grouped tensor in the padded layout:
+    per group, its amaxes and its rows quantized at their padded positions.
+    The columnwise direction quantizes the group's rows padded with zero rows
+    to a multiple of 128, all of its 16-row blocks (with RHT a block of pad
+    rows transforms to signed zeros, which keep their sign)."""
+    K = xb.shape[1]
+    starts, P = _pad_starts(sizes)
+    rc = np.zeros((P, K // 2), np.uint8)
+    rs = np.zeros((P, K // 16), np.uint8)
+    cc = np.zeros((K, P // 2), np.uint8)
+    cs = np.zeros((K, P // 16), np.uint8)
+    ar = np.zeros(len(sizes), np.float32)
+    ac = np.zeros(len(sizes), np.float32)
+    src = 0
+    for g, (m, p0) in enumerate(zip(sizes, starts)):
+        if m:
+            xg = xb[src:src + m]
+            ar[g] = oracle.amax(xg)
+            ac[g] = oracle.amax_rht_col(xg, rht) if rht is not None else oracle.amax(xg)
+            c, sc = oracle.nvfp4_quantize_rows_at(xg, float(ar[g]), p0, sr=sr)
+            rc[p0:p0 + m], rs[p0:p0 + m] = c, sc
+            xp = np.zeros((-(-m // 128) * 128, K), np.uint16)
+            xp[:m] = xg
+            c, sc = oracle.nvfp4_quantize_cols_at(xp, float(ac[g]), p0, P, rht_sign=rht, sr=sr)
+            cc[:, p0 // 2:p0 // 2 + c.shape[1]] = c
+            cs[:, p0 // 16:p0 // 16 + sc.shape[1]] = sc
+        src += m
+    return (rc, rs, ar), (cc, cs, ac)
+
+
+@pytest.mark.parametrize("rht,sr", [(True, True), (False, True), (True, False)])
+def test_grouped_nvfp4_sr_rht_operands(rht, sr):
+    """Grouped NVFP4 rows and columns with SR and / or RHT, bit for bit per
+    group (amaxes, codes, swizzled scales), empty and ragged groups included."""
+    x = inputs.student_t3_outliers(sum(SIZES), 256)
+    sign = inputs.rht_sign_vector() if rht else None
+    srv = (inputs.SR_SEED, 5) if sr else None
+    xr, xc = nvq.grouped_hybrid_quantize(x.cuda(), SIZES, nvq.NVFP4, nvq.NVFP4, rht_sign=sign, sr=srv)
+    torch.cuda.synchronize()
+    (rc, rs, ar), (cc, cs, ac) = _grouped_nvfp4_oracle(bits(x), SIZES, sign, srv)
+    assert np.array_equal(xr.amax.cpu().numpy(), ar), "row amaxes"
+    assert np.array_equal(xc.amax.cpu().numpy(), ac), "column amaxes"
+    assert_codes_equal(qt_codes(xr), rc, "grouped rows codes")
+    assert_scales_equal(xr, rs, "grouped rows scales")
+    assert_codes_equal(qt_codes(xc), cc, "grouped cols codes")
+    assert_scales_equal(xc, cs, "grouped cols scales")
+
+
+def test_grouped_nvfp4_backward_sr_rht():
+    """A grouped NVFP4 backward: dgrad dx_g = dy_g W_g with dy SR-quantized,
+    wgrad dW_g = dy_g^T x_g with both operands RHT'd (the transform cancels)
+    and dy SR-quantized; each against the oracle's fp64 product of its own
+    dequantized operands."""
+    x, w, dy = _setup(SIZES)
+    G, N, K = w.shape
+    sign = inputs.rht_sign_vector()
+    srv = (inputs.SR_SEED, 0)
+    dyr, dyc = nvq.grouped_hybrid_quantize(dy.cuda(), SIZES, nvq.NVFP4, nvq.NVFP4, rht_sign=sign, sr=srv)
+    _, xc = nvq.grouped_hybrid_quantize(x.cuda(), SIZES, nvq.NONE, nvq.NVFP4, rht_sign=sign)
+    _, wc = nvq.grouped_hybrid_quantize(w.reshape(G * N, K).cuda(), [N] * G, nvq.NONE, nvq.NVFP4)
+    dx = nvq.grouped_gemm_rows(dyr, wc, SIZES, N, b_col_groups=True)
+    dw = nvq.grouped_gemm_wgrad(dyc, xc, SIZES)
+    torch.cuda.synchronize()
+    (drc, drs, dar), (dcc, dcs, dac) = _grouped_nvfp4_oracle(bits(dy), SIZES, sign, srv)
+    _, (xcc, xcs, xac) = _grouped_nvfp4_oracle(bits(x), SIZES, sign, None)
+    assert_codes_equal(qt_codes(dyr), drc, "dy rows codes")
+    assert_codes_equal(qt_codes(dyc), dcc, "dy cols codes")
+    assert_codes_equal(qt_codes(xc), xcc, "x cols codes")
+    starts, P = _pad_starts(SIZES)
+    wb = bits(w)
+    src = 0
+    for g, (m, p0) in enumerate(zip(SIZES, starts)):
+        if m == 0:
+            assert torch.count_nonzero(dw[g]).item() == 0
+            continue
+        wcc, wcs, wa = oracle.nvfp4_quantize_cols(wb[g])  # [K][N]
+        a = oracle.nvfp4_dequant(drc[p0:p0 + m], drs[p0:p0 + m], oracle.nvfp4_g(float(dar[g])))
+        assert_gemm_close(dx[src:src + m], oracle.gemm_tn_f64(a, oracle.nvfp4_dequant(wcc, wcs, oracle.nvfp4_g(wa))),
+                          f"group {g} dgrad")
+        mp = -(-m // 128) * 128
+        da = oracle.nvfp4_dequant(dcc[:, p0 // 2:(p0 + mp) // 2], dcs[:, p0 // 16:(p0 + mp) // 16],
+                                  oracle.nvfp4_g(float(dac[g])))
+        xa = oracle.nvfp4_dequant(xcc[:, p0 // 2:(p0 + mp) // 2], xcs[:, p0 // 16:(p0 + mp) // 16],
+                                  oracle.nvfp4_g(float(xac[g])))
+        # a group of fewer than 16 tokens contracts over one Hadamard block:
+        # every output is a short sum with heavy cancellation, so a few more
+        # elements land 2 bf16 ulps from the fp64 value (the Frobenius bar holds)
+        assert_gemm_close(dw[g], oracle.gemm_tn_f64(da, xa), f"group {g} wgrad", ulp_frac=0.999 if m >= 16 else 0.99)
+        src += m
