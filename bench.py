@@ -183,7 +183,40 @@ def oracle_single_thread(target_s=6.0):
         return None, f"single-thread oracle run failed: {type(e).__name__}"
 
 
+def oracle_sweep_rate(Ms):
+    """The oracle (every OpenMP thread of this process) on the quantize sweep's
+    tensors of M in Ms: per tensor the amax and row + col quantization of the
+    three variants (NVFP4 RTN, NVFP4 with RHT and SR, MXFP8), input generation
+    not timed.  Returns (GB/s of the sweep's algorithmic bytes, seconds)."""
+    import numpy as np
+    import torch
+    import oracle
+    from mxfp8_block_scaled_bf16_gb300 import inputs
+    sign = inputs.rht_sign_vector()
+    sr = (inputs.SR_SEED, 0)
+    tot_b = tot_s = 0.0
+    for Mq in Ms:
+        xb = inputs.student_t3_outliers(Mq).contiguous().view(torch.int16).numpy().view(np.uint16)
+        t0 = time.perf_counter()
+        A = oracle.amax(xb)
+        oracle.nvfp4_quantize_rows(xb, A=A)
+        oracle.nvfp4_quantize_cols(xb)
+        oracle.nvfp4_quantize_rows(xb, A=A, sr=sr)
+        oracle.nvfp4_quantize_cols(xb, rht_sign=sign, sr=sr)
+        oracle.mxfp8_quantize_rows(xb)
+        oracle.mxfp8_quantize_cols(xb)
+        tot_s += time.perf_counter() - t0
+        tot_b += xb.size * (5.125 + 5.125 + 4.0625)
+    return tot_b / tot_s / 1e9, tot_s
+
+
 def _oracle_child(target_s):
+    if target_s < 0:  # the quantize sweep's single-thread figure, on its smallest tensor
+        from mxfp8_block_scaled_bf16_gb300 import inputs
+        Ms = [min(inputs.QUANT_SWEEP_M)]
+        v, secs = oracle_sweep_rate(Ms)
+        print(json.dumps({"value": v, "sample": f"sweep tensor M={Ms[0]}, measured {secs:.2f} s"}), flush=True)
+        return 0
     from mxfp8_block_scaled_bf16_gb300 import inputs
     x, w, dy = inputs.llama_up()
     v, desc, threads, _ = oracle_sample(x, w, dy, inputs.rht_sign_vector(), target_s=target_s)
@@ -576,10 +609,22 @@ def run_quant_sweep(args, nvq, inputs):
         del x, nr, nc, mr, mc
         torch.cuda.empty_cache()
     value = tot_b / (tot_ms * 1e-3) / 1e9
-    return {"metric": "quantize sweep GB/s (algorithmic bytes, NVFP4 RTN / RHT+SR / MXFP8, row+col)",
+    line = {"metric": "quantize sweep GB/s (algorithmic bytes, NVFP4 RTN / RHT+SR / MXFP8, row+col)",
             "value": value, "unit": "GB/s", "ms_per_step": tot_ms, "dtype": "bf16 -> nvfp4 / mxfp8",
             "config": {"workload": "quantize_sweep_Mx4096_student_t3", "M": list(inputs.QUANT_SWEEP_M), "K": 4096},
             "sweep": entries, "roofline_bound": "hbm", "step_bytes": tot_b}
+    if not args.no_cpu_baseline:
+        # the oracle on the full sweep tensors with every host core, and with
+        # one thread (a child process) on the smallest tensor
+        cpu_v, cpu_s = oracle_sweep_rate(inputs.QUANT_SWEEP_M)
+        threads = _env_int("OMP_NUM_THREADS", os.cpu_count() or 1)
+        st_v, st_desc = oracle_single_thread(-1.0)
+        line["cpu_baseline"] = {
+            "value": cpu_v, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"the full sweep tensors (M = {list(inputs.QUANT_SWEEP_M)}, three variants), measured {cpu_s:.1f} s",
+            "extrapolated": False,
+            "single_thread": {"value": st_v, "unit": "GB/s", "cores": 1, "sample": st_desc, "extrapolated": False}}
+    return line
 
 
 def run_moe_grouped(args, nvq, inputs):
