@@ -814,6 +814,8 @@ def run_variants(args, nvq, inputs):
                    forward GEMM with a row-scaled A vs a per-group-scaled A
       two_d        W: MXFP8 rows + NVFP4 columns with 16x16 tile scales vs 1x16 blocks
       hybrid_linear  MXFP8 forward + NVFP4 backward step (W columns 2D) vs the NVFP4 step
+      grouped_nvfp4_bwd  MoE workload, NVFP4 backward: dy rows + columns with SR (columns with
+                   RHT), x and W columns (x with RHT), grouped NVFP4 dgrad and wgrad
 
     Quantize rates are algorithmic bytes (each pass's bf16 read + the outputs written) per
     second; GEMM / step rates are FLOPs per second.  Inputs above L2 are timed back to back
@@ -898,7 +900,7 @@ def run_variants(args, nvq, inputs):
     del hb, ybuf, dxb, dwb, y, x, w, dy, xr, xcol, wr
     torch.cuda.empty_cache()
     # ---- f-3: row-scaled NVFP4 on the MoE workload
-    sizes, xm, wm, _ = inputs.moe_grouped()
+    sizes, xm, wm, dyh_m = inputs.moe_grouped()
     sizes = [int(v) for v in sizes]
     G, Nn, Km = wm.shape
     xm = xm.cuda()
@@ -923,6 +925,43 @@ def run_variants(args, nvq, inputs):
                          "grouped_fwd_row_scaled_ms": tgr, "grouped_fwd_row_scaled_TFLOP/s": mflop / (tgr * 1e-3) / 1e12,
                          "grouped_fwd_per_group_ms": tgp, "grouped_fwd_per_group_TFLOP/s": mflop / (tgp * 1e-3) / 1e12,
                          "bytes_per_element": brs}
+    del xrs, xrp, xcm, wrg, ym
+    torch.cuda.empty_cache()
+    # ---- grouped NVFP4 backward on the MoE workload
+    dym = dyh_m.cuda()
+    del dyh_m
+    dyr, dyc = al(nvq.NVFP4, P, Nn, n_amax=G), al(nvq.NVFP4, Nn, P, n_amax=G)
+    xcn, wcn = al(nvq.NVFP4, Km, P, n_amax=G), al(nvq.NVFP4, Km, G * Nn, n_amax=G)
+    dxm = torch.empty(T, Km, dtype=torch.bfloat16, device="cuda")
+    dwm = torch.empty(G, Nn, Km, dtype=torch.bfloat16, device="cuda")
+
+    def q_dy():
+        nvq.grouped_hybrid_quantize(dym, sizes, nvq.NVFP4, nvq.NVFP4, out_row=dyr, out_col=dyc, rht_sign=sign, sr=sr)
+
+    def q_x():
+        nvq.grouped_hybrid_quantize(xm, sizes, nvq.NONE, nvq.NVFP4, out_col=xcn, rht_sign=sign)
+
+    def q_w():
+        nvq.grouped_hybrid_quantize(w2, [Nn] * G, nvq.NONE, nvq.NVFP4, out_col=wcn)
+
+    def dgrad():
+        nvq.grouped_gemm_rows(dyr, wcn, sizes, Nn, b_col_groups=True, out=dxm)
+
+    def wgrad():
+        nvq.grouped_gemm_wgrad(dyc, xcn, sizes, out=dwm)
+
+    def bwd():
+        q_dy(); q_x(); q_w(); dgrad(); wgrad()
+
+    bwd()
+    tqd, tqx, tqw = timed(q_dy, 1e12), timed(q_x, 1e12), timed(q_w, 1e12)
+    tdg, twg, tbw = timed(dgrad, 1e12), timed(wgrad, 1e12), _graph_ms(bwd, args.steps, args.warmup)
+    out["grouped_nvfp4_bwd"] = {
+        "quantize_ms": {"dy_row_col_sr_rht": tqd, "x_col_rht": tqx, "w_col": tqw},
+        "dgrad_ms": tdg, "dgrad_TFLOP/s": mflop / (tdg * 1e-3) / 1e12,
+        "wgrad_ms": twg, "wgrad_TFLOP/s": mflop / (twg * 1e-3) / 1e12,
+        "bwd_step_ms": tbw, "bwd_TFLOP/s": 2 * mflop / (tbw * 1e-3) / 1e12,
+        "note": "the quantizations with their amax passes; dgrad dx_g = dy_g W_g, wgrad dW_g = dy_g^T x_g"}
     peaks, src = _peaks()
     return {"metric": "recipe variants (amax chain, rowwise-dequantized source, row scaling, 2D scaling, hybrid linear)",
             "value": out["hybrid_linear"]["TFLOP/s"], "unit": "TFLOP/s (hybrid-format linear step)",
