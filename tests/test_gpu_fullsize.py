@@ -145,3 +145,67 @@ def test_moe_grouped_full_size():
         assert np.array_equal(xc_s[:, p0 // 32:(p0 + mp) // 32], wbb[1]), f"expert {g} x_col scales"
         rows, cols = _sample_positions(Nn, K, 512, 30 + g)
         _check_sampled(dw[g].cpu(), 2, wa, wbb, mp, rows, cols, f"expert {g} wgrad")
+
+
+def test_moe_grouped_nvfp4_backward_full_size():
+    """The MoE workload with an NVFP4 backward ("MXFP8 fwd and NVFP4 bwd (or vice
+    versa)"): dy grouped with SR in both directions and RHT on the columns, x
+    columns with RHT, W columns; grouped NVFP4 dgrad and wgrad.  For a spread of
+    experts the operands are bit-exact against the oracle at their padded
+    positions (the stochastic-rounding index of a grouped element), and sampled
+    outputs are within the GEMM tolerance."""
+    sizes, x, w, dy = inputs.moe_grouped()
+    G, Nn, K = w.shape
+    sizes = [int(v) for v in sizes]
+    sign = inputs.rht_sign_vector()
+    sr = (inputs.SR_SEED, 0)
+    dyr, dyc = nvq.grouped_hybrid_quantize(dy.cuda(), sizes, nvq.NVFP4, nvq.NVFP4, rht_sign=sign, sr=sr)
+    _, xc = nvq.grouped_hybrid_quantize(x.cuda(), sizes, nvq.NONE, nvq.NVFP4, rht_sign=sign)
+    _, wc = nvq.grouped_hybrid_quantize(w.reshape(G * Nn, K).cuda(), [Nn] * G, nvq.NONE, nvq.NVFP4)
+    dx = nvq.grouped_gemm_rows(dyr, wc, sizes, Nn, b_col_groups=True)
+    dw = nvq.grouped_gemm_wgrad(dyc, xc, sizes)
+    torch.cuda.synchronize()
+
+    order = np.argsort(sizes)
+    picks = sorted(set([int(order[0]), int(order[1]), int(order[-1]), int(order[len(order) // 2]), 9]))
+    offs = np.concatenate([[0], np.cumsum(sizes)])
+    poffs = np.concatenate([[0], np.cumsum([-(-m // 128) * 128 for m in sizes])])
+    P = int(poffs[-1])
+    xb, wb, dyb = bits(x), bits(w), bits(dy)
+    dyr_c, dyc_c, xc_c, wc_c = qt_codes(dyr), qt_codes(dyc), qt_codes(xc), qt_codes(wc)
+    dyr_s = oracle.scale_unswizzle(qt_scales(dyr), P, Nn // 16)
+    dyc_s = oracle.scale_unswizzle(qt_scales(dyc), Nn, P // 16)
+    xc_s = oracle.scale_unswizzle(qt_scales(xc), K, P // 16)
+    wc_s = oracle.scale_unswizzle(qt_scales(wc), K, G * Nn // 16)
+    for g in picks:
+        m, s0, p0 = sizes[g], int(offs[g]), int(poffs[g])
+        mp = -(-m // 128) * 128
+        # W_g columns (contraction N), as dgrad's B operand
+        wcc, wcs, wa = oracle.nvfp4_quantize_cols(wb[g])
+        assert wc.amax[g].item() == np.float32(wa), f"expert {g} w_col amax"
+        assert_codes_equal(wc_c[:, g * Nn // 2:(g + 1) * Nn // 2], wcc, f"expert {g} w_col codes")
+        assert np.array_equal(wc_s[:, g * Nn // 16:(g + 1) * Nn // 16], wcs), f"expert {g} w_col scales"
+        # dy_g rows (SR) at padded rows p0..
+        dg = dyb[s0:s0 + m]
+        A_r = oracle.amax(dg)
+        assert dyr.amax[g].item() == np.float32(A_r), f"expert {g} dy_row amax"
+        rc, rs = oracle.nvfp4_quantize_rows_at(dg, A_r, p0, sr=sr)
+        assert_codes_equal(dyr_c[p0:p0 + m], rc, f"expert {g} dy_row codes")
+        assert np.array_equal(dyr_s[p0:p0 + m], rs), f"expert {g} dy_row scales"
+        # dy_g and x_g columns (RHT; SR for dy) over the zero-padded group
+        dp = np.zeros((mp, Nn), np.uint16); dp[:m] = dg
+        xp = np.zeros((mp, K), np.uint16); xp[:m] = xb[s0:s0 + m]
+        A_dc, A_xc = oracle.amax_rht_col(dg, sign), oracle.amax_rht_col(xb[s0:s0 + m], sign)
+        assert dyc.amax[g].item() == np.float32(A_dc), f"expert {g} dy_col amax"
+        assert xc.amax[g].item() == np.float32(A_xc), f"expert {g} x_col amax"
+        dcc, dcs = oracle.nvfp4_quantize_cols_at(dp, A_dc, p0, P, rht_sign=sign, sr=sr)
+        xcc, xcs = oracle.nvfp4_quantize_cols_at(xp, A_xc, p0, P, rht_sign=sign)
+        assert_codes_equal(dyc_c[:, p0 // 2:(p0 + mp) // 2], dcc, f"expert {g} dy_col codes")
+        assert np.array_equal(dyc_s[:, p0 // 16:(p0 + mp) // 16], dcs), f"expert {g} dy_col scales"
+        assert_codes_equal(xc_c[:, p0 // 2:(p0 + mp) // 2], xcc, f"expert {g} x_col codes")
+        assert np.array_equal(xc_s[:, p0 // 16:(p0 + mp) // 16], xcs), f"expert {g} x_col scales"
+        # sampled outputs from the oracle's own operands
+        rows, cols = _sample_positions(m, K, 512, 30 + g)
+        _check_sampled(dx[s0:s0 + m].cpu(), 1, (rc, rs, A_r), (wcc, wcs, wa), Nn, rows, cols, f"expert {g} dgrad")
+        rows, cols = _sample_positions(Nn, K, 512, 40 + g)
+        _check_sampled(dw[g].cpu(), 1, (dcc, dcs, A_dc), (xcc, xcs, A_xc), mp, rows, cols, f"expert {g} wgrad")
