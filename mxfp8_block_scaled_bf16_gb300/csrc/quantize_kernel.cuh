@@ -285,7 +285,8 @@ __device__ __forceinline__ uint32_t nvfp4_block_scale(const Nvfp4Scale& ts, cons
 }
 
 // The same by division (kept for the NVFP4-row + MXFP8-column variant, where
-// the table version made the compiler spill registers).
+// the table version makes the compiler spill registers and runs no faster:
+// that variant is bound by memory, not by this division).
 __device__ __forceinline__ uint32_t nvfp4_block_scale_div(const Nvfp4Scale& ts, float b, float& e)
 {
     uint32_t S = 0;
