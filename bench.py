@@ -303,8 +303,37 @@ def run_ours(args, rank, world, local_rank):
             ev[5].record(stream)
             gemm_events.append(ev)
 
+    side = torch.cuda.Stream(dev)
+
+    def step_overlapped():
+        """The same calls in the same dependency order, with the two independent
+        pairs on two streams: x's and W's quantizations (both feed the forward
+        GEMM), and dgrad / wgrad (disjoint operands), so each can run in the
+        other's last partial wave."""
+        cur = torch.cuda.current_stream(dev)
+        fork = torch.cuda.Event()
+        fork.record(cur)
+        side.wait_event(fork)
+        nvq.nvfp4_quantize(x, 3, rht_sign=sign, out_row=fwd_bufs["x_row"], out_col=fwd_bufs["x_col"], stream=cur)
+        nvq.nvfp4_quantize(w, 3, out_row=fwd_bufs["w_row"], out_col=fwd_bufs["w_col"], stream=side)
+        join = torch.cuda.Event()
+        join.record(side)
+        cur.wait_event(join)
+        nvq.gemm_tn(fwd_bufs["x_row"], fwd_bufs["w_row"], out=y, stream=cur)
+        nvq.nvfp4_linear_bwd_quantize(dy, rht_sign=sign, sr=sr, bufs=bwd_bufs, stream=cur)
+        fork2 = torch.cuda.Event()
+        fork2.record(cur)
+        side.wait_event(fork2)
+        nvq.nvfp4_linear_dgrad(bwd_bufs["dy_row"], fwd_bufs["w_col"], dx=dx, stream=cur)
+        nvq.nvfp4_linear_wgrad(bwd_bufs["dy_col"], fwd_bufs["x_col"], dw=dw, stream=side)
+        join2 = torch.cuda.Event()
+        join2.record(side)
+        cur.wait_event(join2)
+
     for _ in range(args.warmup):
         step(False)
+        if not args.serial_step:
+            step_overlapped()
     torch.cuda.synchronize()
     if nvq.device_status() != 0:
         raise RuntimeError("device status error during warm-up")
@@ -316,7 +345,10 @@ def run_ours(args, rank, world, local_rank):
     if not args.eager:
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph):
-            step(False)
+            if args.serial_step:
+                step(False)
+            else:
+                step_overlapped()
         torch.cuda.synchronize()
         for _ in range(args.warmup):
             graph.replay()
@@ -388,6 +420,8 @@ def run_ours(args, rank, world, local_rank):
         "vs_baseline": None, "dtype": "nvfp4", "data": "synthetic", "config": CONFIG,
         "gpu_launches": 9 * args.steps,
         "launch_mode": "eager" if args.eager else "cuda_graph",
+        "step_schedule": "one stream" if (args.eager or args.serial_step) else
+                         "two streams: x / W quantization, then dgrad / wgrad, side by side",
         "roofline": {"bound": "tensor", "kernel": gemm_label,
                      "achieved": achieved, "peak": peak_fp4, "unit": "TFLOP/s", "frac": achieved / peak_fp4,
                      "traffic": GEMM_TRAFFIC_BYTES if pair else None,
@@ -1026,6 +1060,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end measurement")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip timing the CPU oracle")
     ap.add_argument("--eager", action="store_true", help="launch the step eagerly instead of replaying a CUDA graph")
+    ap.add_argument("--serial-step", action="store_true",
+                    help="replay the step's calls on one stream (default: the two independent pairs on two streams)")
     ap.add_argument("--oracle-child", type=float, default=None, help=argparse.SUPPRESS)
     ap.add_argument("--no-amax-chain", action="store_true",
                     help="qwen3_stack: measure every amax with its own pass instead of taking it from the producing GEMM")
